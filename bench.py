@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark: routed MoE EP dispatch + combine on one GB300 (W ranks in HBM).
+
+One step = one dispatch (routing/slot kernel + fused a1->batched row mover)
+and one combine (weighted gather-reduce) over the whole batch of all W
+simulated ranks, with identity experts (expert_out = b_a1). Prints one JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3] [--impl ours|reference]
+
+With N > 1 (under torch.distributed.run) every rank runs an independent
+replica of the workload: the path has no data exchange between GPUs here, so
+nothing is sharded and no collective touches the data; the ranks only meet at
+the barriers around the timed region and in the max-over-ranks of its time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from combine_ep_route_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and effective HBM GB/s (fraction of peak), 1 GB300"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="fused", choices=["fused", "sendbuf"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def workload_counts(x: wl.Workload):
+    """Exact counts of the algorithmic byte formula from the drawn inputs."""
+    ids = x.topk_ids
+    W, T, K = ids.shape
+    live = np.arange(T)[None, :] < x.num_tokens[:, None]
+    kept = (ids >= 0) & live[:, :, None]
+    n_pairs = int(kept.sum())
+    n_tok_routed = int(kept.any(axis=2).sum())
+    n_tok = int(x.num_tokens.sum())
+    return n_pairs, n_tok_routed, n_tok
+
+
+def algorithmic_bytes(x: wl.Workload, out_bytes_per_elem: int = 2):
+    """(dispatch bytes, combine bytes): each routed token row (+ extras) read
+    once and written once per pair; each pair row read once and each output row
+    written once. Metadata (ids, weights, maps; < 1 %) is not counted."""
+    s = x.spec
+    n_pairs, n_tok_routed, n_tok = workload_counts(x)
+    bx = 2 * s.h
+    bp = sum(x.extra_row_bytes)
+    disp = (bx + bp) * (n_tok_routed + n_pairs)
+    comb = bx * n_pairs + out_bytes_per_elem * s.h * n_tok
+    return disp, comb
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_ep_route_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, cfg: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    src = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if (parts.get("kernel") == kernel and parts.get("config") == str(cfg)
+                    and parts.get("source") == src and "bytes_per_launch" in parts):
+                return float(parts["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/ep_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [v.strip() for v in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    mx = float(c[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def replica_aggregate(ms_local: float, tokens_local: int, dist=None, device=None):
+    """Whole-job figures of N independent replicas: the step time is the max over
+    ranks, the tokens are summed over ranks. Returns (ms, tokens, tokens/s)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms_local, tokens_local, tokens_local / (ms_local * 1e-3)
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    ms, tok = float(t.item()), int(n.item())
+    return ms, tok, tok / (ms * 1e-3)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ CPU oracle legs
+
+def oracle_step(x: wl.Workload):
+    from oracle import ref
+    s = x.spec
+    m = ref.dispatch_meta(s.W, s.E, s.K, s.T, x.topk_ids, x.topk_weights, x.num_tokens)
+    rows = ref.dispatch_rows(m, x.a1)
+    ref.combine(m, x.topk_weights, rows)
+    return int(x.num_tokens.sum())
+
+
+def cpu_baseline(cfg: int, budget_s: float = 12.0):
+    """The oracle as it stands (one host thread) on the full workload, repeated
+    until about budget_s of CPU work."""
+    x = wl.make(cfg)
+    toks, t_all, reps = 0, 0.0, 0
+    while t_all < budget_s and reps < 3:
+        t0 = time.perf_counter()
+        toks += oracle_step(x)
+        t_all += time.perf_counter() - t0
+        reps += 1
+    return {"value": toks / t_all, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full step(s) of {x.spec.name} ({toks} tokens) on one host thread, "
+                      f"{t_all:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    full = wl.spec(args.config)
+    per_step_budget = min(0.25, 150.0 / max(1, args.steps + args.warmup))
+    # size the per-step sample: tokens per rank so one oracle step fits the budget
+    T = 8
+    x = wl.make(wl.spec(args.config, T=T))
+    t0 = time.perf_counter()
+    oracle_step(x)
+    dt = time.perf_counter() - t0
+    T = max(1, min(full.T, int(T * per_step_budget / max(dt, 1e-6))))
+    x = wl.make(wl.spec(args.config, T=T))
+    for _ in range(args.warmup):
+        oracle_step(x)
+    toks = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        toks += oracle_step(x)
+    el = time.perf_counter() - t0
+    v = toks / el
+    sample = (f"each step: the oracle on {full.name} with {T} tokens per rank "
+              f"({x.spec.W * T} tokens, same generators), one host thread")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": full.name, "W": full.W, "E": full.E, "top_k": full.K,
+                       "tokens_per_rank": full.T, "hidden": full.h, "path": "oracle"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from combine_ep_route_gb300 import EpConfig, EpContext, _lib as L
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    x = wl.make(args.config)
+    s = x.spec
+    cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(x.extra_row_bytes),
+                   sendbuf=args.path == "sendbuf")
+    ctx = EpContext(cfg, dev)
+    a1 = torch.from_numpy(x.a1.view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(x.topk_ids).to(dev)
+    w = torch.from_numpy(x.topk_weights).to(dev)
+    nt = torch.from_numpy(x.num_tokens).to(dev)
+    extras = [torch.from_numpy(e).to(dev) for e in x.extras]
+    out = ctx.alloc_dispatch_outputs()
+    y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
+        ctx.combine(out.b_a1, out=y)
+
+    ctx.set_option(L.EP_OPT_KERNEL_TIMING, 1)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    ctx.check()
+    ctx.kernel_times()   # drop warm-up records
+
+    n = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(n):
+            flush.zero_()                    # L2 flush between steps (not timed)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    st = ctx.status()
+    if st != 0:
+        raise SystemExit(f"device status {st} after the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kt = ctx.kernel_times()
+    clocks = clk.summary()
+    disp_b, comb_b = algorithmic_bytes(x)
+    n_pairs, n_tok_routed, n_tok = workload_counts(x)
+    ms, _, value = replica_aggregate(sum(step_ms) / n, n_tok, dist if world > 1 else None, dev)
+    peak, peak_src = measured_peaks()
+    # per-kernel durations (CUDA events around every launch, on the launch stream)
+    per = {}
+    for name in ("route", "move_fused", "pack", "exchange", "deliver", "combine"):
+        launches, tot, timed = kt[name]
+        if timed:
+            per[name] = tot / timed
+    dom = max(("move_fused", "combine"), key=lambda k: per.get(k, 0.0)) if args.path == "fused" else "combine"
+    dom_bytes = disp_b if dom == "move_fused" else comb_b
+    achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
+    traffic = traffic_for(dom, args.config)
+    launches = int(sum(v[0] for v in kt.values()))
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ctx, x, dev, out, n, stream)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.config)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": s.name, "W": s.W, "E": s.E, "top_k": s.K, "tokens_per_rank": s.T,
+                   "hidden": s.h, "extra_row_bytes": list(x.extra_row_bytes), "path": args.path,
+                   "out_dtype": "bf16", "accumulate": "f32", "experts": "identity (expert_out = b_a1)",
+                   "l2": "flushed: 256 MiB write before every step, outside the step's events",
+                   "replicas": world},
+        "effective_gbs": (disp_b + comb_b) / (ms * 1e-3) / 1e9,
+        "effective_frac_of_peak": (disp_b + comb_b) / (ms * 1e-3) / 1e9 / peak,
+        "alg_bytes_per_step": {"dispatch": disp_b, "combine": comb_b},
+        "counts": {"pairs": n_pairs, "tokens_routed": n_tok_routed, "tokens": n_tok},
+        "kernel_ms": {k: round(v, 5) for k, v in per.items()},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(ctx, x, dev, out, n, stream):
+    """Same metric through the public API from pinned host buffers: every step
+    copies its inputs host->device, dispatches, combines, and copies the output
+    back, all inside the timed region."""
+    import torch
+    s = x.spec
+    h_a1 = torch.from_numpy(x.a1.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_ids = torch.from_numpy(x.topk_ids).pin_memory()
+    h_w = torch.from_numpy(x.topk_weights).pin_memory()
+    h_ex = [torch.from_numpy(e).pin_memory() for e in x.extras]
+    h_y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16).pin_memory()
+    d_a1 = torch.empty_like(h_a1, device=dev)
+    d_ids = torch.empty_like(h_ids, device=dev)
+    d_w = torch.empty_like(h_w, device=dev)
+    d_ex = [torch.empty_like(e, device=dev) for e in h_ex]
+    d_y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in [h_a1, h_ids, h_w, *h_ex])
+    d2h = h_y.numel() * h_y.element_size()
+
+    def step():
+        d_a1.copy_(h_a1, non_blocking=True)
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        for d, h in zip(d_ex, h_ex):
+            d.copy_(h, non_blocking=True)
+        ctx.dispatch(d_a1, d_ids, d_w, extras=d_ex, out=out)
+        ctx.combine(out.b_a1, out=d_y)
+        h_y.copy_(d_y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    m = max(10, min(n, 100))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(m):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / m
+    ctx.kernel_times()
+    tokens = int(x.num_tokens.sum())
+    return {"value": tokens / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": m,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "EpContext.dispatch/combine with pinned host copies"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,551 @@
+// api.cu -- the C-ABI of the EP dispatch/combine library (declared in
+// include/ep.h): configuration checks, workspace layout, the dispatch/combine
+// state rule, kernel launches on the caller's stream, status readback and the
+// per-kernel event timing used by the benchmark.
+#include "ep_internal.cuh"
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+using ep::Layout;
+
+namespace {
+
+constexpr int kIdle = 0, kDispatched = 1;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool config_ok(const ep_config_t *c) {
+    if (!c) return false;
+    if (c->W < 1 || c->W > EP_MAX_W) return false;
+    if (c->E < c->W || c->E > EP_MAX_E || c->E % c->W != 0) return false;
+    if (c->top_k < 1 || c->top_k > EP_MAX_TOPK || c->top_k > c->E) return false;
+    if (c->max_tokens < 1 || c->hidden < 8 || (2LL * c->hidden) % 16 != 0) return false;
+    if (c->x_dtype != EP_BF16) return false;
+    if (c->n_extra < 0 || c->n_extra > EP_MAX_EXTRA) return false;
+    long long rb = 2LL * c->hidden;
+    for (int i = 0; i < c->n_extra; ++i) {
+        if (c->extra_row_bytes[i] <= 0 || c->extra_row_bytes[i] % 16 != 0) return false;
+        rb += c->extra_row_bytes[i];
+    }
+    if (c->flags & ~(EP_FLAG_ZERO_PAD | EP_FLAG_SENDBUF)) return false;
+    // a row must fit twice into one mover CTA's stage memory
+    if (2 * align_up((size_t)rb, 128) > ep::kMoveSmemBudget) return false;
+    // flat expert row indices (E * Ecap) and flat pair indices stay within int32
+    const long long ecap = (long long)c->max_tokens * c->W;
+    if ((long long)c->E * ecap >= (1LL << 31)) return false;
+    if ((long long)c->W * c->W * c->max_tokens * c->top_k >= (1LL << 31)) return false;
+    return true;
+}
+
+void compute_layout(const ep_config_t *c, Layout *L) {
+    const int W = c->W, Tm = c->max_tokens, K = c->top_k;
+    L->e_local = c->E / W;
+    L->S = K < L->e_local ? K : L->e_local;
+    L->Ecap = Tm * W;
+    L->tiles_per_rank = (Tm + ep::kRouteTile - 1) / ep::kRouteTile;
+    L->num_tiles = W * L->tiles_per_rank;
+    L->n_ctr = W + c->E;
+    uint32_t rb = 2u * (uint32_t)c->hidden;
+    for (int i = 0; i < c->n_extra; ++i) rb += (uint32_t)c->extra_row_bytes[i];
+    L->row_bytes = rb;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, ep::kAlign);
+        return at;
+    };
+    const size_t pairs = (size_t)W * Tm * K;
+    const size_t slots = (size_t)W * W * Tm * L->S;
+    L->hdr = take(sizeof(ep::DevHeader));
+    L->tile_flag = take((size_t)L->num_tiles * 4);
+    L->tile_agg = take((size_t)L->num_tiles * L->n_ctr * 4);
+    L->tile_incl = take((size_t)L->num_tiles * L->n_ctr * 4);
+    L->send_cnt = take((size_t)W * W * 4);
+    L->pair_row = take(pairs * 4);
+    L->pair_w = take(pairs * 4);
+    L->pair_send = take(pairs * 4);
+    L->recv_eloc = take(slots * 4);
+    L->recv_w = take(slots * 4);
+    L->recv_row = take(slots * 4);
+    if (c->flags & EP_FLAG_SENDBUF) {
+        L->send_x = take((size_t)W * W * Tm * rb);
+        L->recv_x = take((size_t)W * W * Tm * rb);
+    } else {
+        L->send_x = L->recv_x = (size_t)-1;
+    }
+    L->total = off;
+}
+
+}  // namespace
+
+struct ep_ctx {
+    ep_config_t cfg;
+    Layout L;
+    uint8_t *ws;
+    size_t ws_bytes;
+    int state;
+    bool initialized;
+    int num_sms;
+    uint32_t epoch;
+    // options
+    uint64_t wait_limit_ns;
+    int timing;
+    int pdl;
+    int move_ctas_per_sm;
+    int move_pipes;
+    int fault_skip;
+    int combine_ctas_per_sm;
+    // counters and event timing
+    int64_t launches[EP_K_COUNT];
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[EP_K_COUNT];
+    std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+template <class T>
+T *ws_ptr(const ep_ctx *c, size_t off) {
+    return reinterpret_cast<T *>(c->ws + off);
+}
+
+cudaEvent_t take_event(ep_ctx *c) {
+    if (!c->pool.empty()) {
+        cudaEvent_t e = c->pool.back();
+        c->pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Records an event pair around one kernel launch when timing is on.
+struct KernelTimer {
+    ep_ctx *c;
+    int kind;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr, b = nullptr;
+    KernelTimer(ep_ctx *c_, int kind_, cudaStream_t st_) : c(c_), kind(kind_), st(st_) {
+        c->launches[kind]++;
+        if (c->timing) {
+            a = take_event(c);
+            b = take_event(c);
+            if (a) cudaEventRecord(a, st);
+        }
+    }
+    ~KernelTimer() {
+        if (a && b) {
+            cudaEventRecord(b, st);
+            c->pending[kind].emplace_back(a, b);
+        } else {
+            if (a) c->pool.push_back(a);
+            if (b) c->pool.push_back(b);
+        }
+    }
+};
+
+int lazy_init(ep_ctx *c, cudaStream_t st) {
+    if (c->initialized) return EP_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return EP_ERR_CUDA;
+    // header and tile flags start at zero; the rest is written before it is read
+    if (cudaMemsetAsync(c->ws, 0, c->L.tile_agg, st) != cudaSuccess) return EP_ERR_CUDA;
+    c->initialized = true;
+    return EP_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+void fill_move_common(const ep_ctx *c, ep::MoveParams &m) {
+    const ep_config_t &cf = c->cfg;
+    std::memset(&m, 0, sizeof(m));
+    m.W = cf.W;
+    m.K = cf.top_k;
+    m.Tm = cf.max_tokens;
+    m.S = c->L.S;
+    m.e_local = c->L.e_local;
+    m.Ecap = c->L.Ecap;
+    m.n_seg = 1 + cf.n_extra;
+    m.seg_bytes[0] = 2u * (uint32_t)cf.hidden;
+    m.seg_off[0] = 0;
+    for (int i = 0; i < cf.n_extra; ++i) {
+        m.seg_bytes[1 + i] = (uint32_t)cf.extra_row_bytes[i];
+        m.seg_off[1 + i] = m.seg_off[i] + m.seg_bytes[i];
+    }
+    m.row_bytes = c->L.row_bytes;
+    m.pair_row = ws_ptr<int32_t>(c, c->L.pair_row);
+    m.pair_send = ws_ptr<int32_t>(c, c->L.pair_send);
+    m.send_cnt = ws_ptr<int32_t>(c, c->L.send_cnt);
+    m.recv_eloc = ws_ptr<int32_t>(c, c->L.recv_eloc);
+    m.recv_row = ws_ptr<int32_t>(c, c->L.recv_row);
+    if (cf.flags & EP_FLAG_SENDBUF) {
+        m.send_x = ws_ptr<uint8_t>(c, c->L.send_x);
+        m.recv_x = ws_ptr<uint8_t>(c, c->L.recv_x);
+    }
+    m.n_tokens = cf.W * cf.max_tokens;
+    m.n_rows = cf.E * c->L.Ecap;
+    m.n_slots = cf.W * cf.W * cf.max_tokens;
+    m.hdr = ws_ptr<ep::DevHeader>(c, c->L.hdr);
+    m.wait_limit_ns = c->wait_limit_ns;
+}
+
+// Pipelines per CTA, stages per pipeline and the dynamic shared memory of one
+// mover CTA for the current options.
+void move_shape(const ep_ctx *c, int &pipes, int &stages, uint32_t &stage_bytes, size_t &smem) {
+    stage_bytes = (uint32_t)align_up(c->L.row_bytes, 128);
+    const int ctas = c->move_ctas_per_sm;
+    size_t budget = ctas == 1 ? ep::kMoveSmemBudget : (size_t)(220 * 1024) / ctas - 2048;
+    if (budget > ep::kMoveSmemBudget) budget = ep::kMoveSmemBudget;
+    int total = (int)(budget / stage_bytes);
+    pipes = c->move_pipes;
+    while (pipes > 1 && total / pipes < 2) --pipes;
+    stages = total / pipes;
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    const int W = c->cfg.W;
+    smem = (size_t)pipes * stages * stage_bytes + (size_t)pipes * stages * 8 +
+           (size_t)pipes * stages * (ep::kMaxDst + 2) * 4 + (size_t)(W * W + 1) * 4;
+}
+
+int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *const *extra_in,
+                     void *b_a1, void *const *extra_out, bool pdl, cudaStream_t st) {
+    ep::MoveParams m;
+    fill_move_common(c, m);
+    m.src_seg[0] = static_cast<const uint8_t *>(a1);
+    m.dst_seg[0] = static_cast<uint8_t *>(b_a1);
+    for (int i = 0; i < c->cfg.n_extra; ++i) {
+        m.src_seg[1 + i] = static_cast<const uint8_t *>(extra_in[i]);
+        m.dst_seg[1 + i] = static_cast<uint8_t *>(extra_out[i]);
+    }
+    int pipes, stages;
+    uint32_t stage_bytes;
+    size_t smem;
+    move_shape(c, pipes, stages, stage_bytes, smem);
+    m.stages = stages;
+    m.stage_bytes = stage_bytes;
+    const int grid = c->num_sms * c->move_ctas_per_sm;
+    KernelTimer tm(c, kind, st);
+    return ep::launch_move(mode, m, grid, pipes * 32, smem, pdl && !c->timing, st) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ep_error_string(int code) {
+    switch (code) {
+        case EP_OK: return "ok";
+        case EP_ERR_INVALID_ARG: return "invalid argument";
+        case EP_ERR_CAPACITY: return "num_tokens outside [0, max_tokens]";
+        case EP_ERR_STATE: return "dispatch/combine called out of order";
+        case EP_ERR_EXPERT_ID: return "expert id >= num_experts (pair dropped)";
+        case EP_ERR_DUPLICATE: return "expert id repeated within a token (later one dropped)";
+        case EP_ERR_TIMEOUT: return "a bounded device wait expired";
+        case EP_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case EP_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int ep_capacities(const ep_config_t *cfg, int32_t *tok_cap, int32_t *slots_per_token,
+                  int32_t *expert_cap) {
+    if (!config_ok(cfg) || !tok_cap || !slots_per_token || !expert_cap) return EP_ERR_INVALID_ARG;
+    const int e_local = cfg->E / cfg->W;
+    *tok_cap = cfg->max_tokens;
+    *slots_per_token = cfg->top_k < e_local ? cfg->top_k : e_local;
+    *expert_cap = cfg->max_tokens * cfg->W;
+    return EP_OK;
+}
+
+int ep_workspace_bytes(const ep_config_t *cfg, size_t *bytes) {
+    if (!config_ok(cfg) || !bytes) return EP_ERR_INVALID_ARG;
+    Layout L;
+    compute_layout(cfg, &L);
+    *bytes = L.total;
+    return EP_OK;
+}
+
+int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_bytes,
+                  ep_ctx_t **out) {
+    if (!config_ok(cfg) || !out) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!d_workspace) return EP_ERR_INVALID_ARG;
+    Layout L;
+    compute_layout(cfg, &L);
+    if (workspace_bytes < L.total || !aligned(d_workspace, ep::kAlign)) return EP_ERR_WORKSPACE;
+    ep_ctx *c = new (std::nothrow) ep_ctx();
+    if (!c) return EP_ERR_INVALID_ARG;
+    c->cfg = *cfg;
+    c->L = L;
+    c->ws = static_cast<uint8_t *>(d_workspace);
+    c->ws_bytes = workspace_bytes;
+    c->state = kIdle;
+    c->initialized = false;
+    c->num_sms = 0;
+    c->epoch = 0;
+    c->wait_limit_ns = 2000000000ull;
+    c->timing = 0;
+    c->pdl = 1;
+    c->move_ctas_per_sm = 1;
+    c->move_pipes = 4;
+    c->fault_skip = -1;
+    c->combine_ctas_per_sm = 8;
+    for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
+    *out = c;
+    return EP_OK;
+}
+
+int ep_ctx_destroy(ep_ctx_t *ctx) {
+    if (!ctx) return EP_OK;
+    for (int k = 0; k < EP_K_COUNT; ++k)
+        for (auto &pr : ctx->pending[k]) {
+            cudaEventDestroy(pr.first);
+            cudaEventDestroy(pr.second);
+        }
+    for (cudaEvent_t e : ctx->pool) cudaEventDestroy(e);
+    delete ctx;
+    return EP_OK;
+}
+
+int ep_ctx_reset(ep_ctx_t *ctx) {
+    if (!ctx) return EP_ERR_INVALID_ARG;
+    ctx->state = kIdle;
+    return EP_OK;
+}
+
+int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
+    if (!ctx) return EP_ERR_INVALID_ARG;
+    switch (option) {
+        case EP_OPT_WAIT_LIMIT_NS:
+            if (value < 1000 || value > 60000000000LL) return EP_ERR_INVALID_ARG;
+            ctx->wait_limit_ns = (uint64_t)value;
+            return EP_OK;
+        case EP_OPT_KERNEL_TIMING:
+            if (value != 0 && value != 1) return EP_ERR_INVALID_ARG;
+            ctx->timing = (int)value;
+            return EP_OK;
+        case EP_OPT_PDL:
+            if (value != 0 && value != 1) return EP_ERR_INVALID_ARG;
+            ctx->pdl = (int)value;
+            return EP_OK;
+        case EP_OPT_MOVE_CTAS_PER_SM:
+            if (value < 1 || value > 4) return EP_ERR_INVALID_ARG;
+            ctx->move_ctas_per_sm = (int)value;
+            return EP_OK;
+        case EP_OPT_MOVE_PIPES:
+            if (value < 1 || value > 8) return EP_ERR_INVALID_ARG;
+            ctx->move_pipes = (int)value;
+            return EP_OK;
+        case EP_OPT_FAULT_SKIP_PUBLISH:
+            if (value < -1 || value >= ctx->L.num_tiles) return EP_ERR_INVALID_ARG;
+            ctx->fault_skip = (int)value;
+            return EP_OK;
+        case EP_OPT_COMBINE_CTAS_PER_SM:
+            if (value < 1 || value > 16) return EP_ERR_INVALID_ARG;
+            ctx->combine_ctas_per_sm = (int)value;
+            return EP_OK;
+        default: return EP_ERR_INVALID_ARG;
+    }
+}
+
+int ep_get_metadata(const ep_ctx_t *ctx, ep_metadata_t *out) {
+    if (!ctx || !out) return EP_ERR_INVALID_ARG;
+    out->send_cnt = ws_ptr<int32_t>(ctx, ctx->L.send_cnt);
+    out->pair_row = ws_ptr<int32_t>(ctx, ctx->L.pair_row);
+    out->pair_w = ws_ptr<float>(ctx, ctx->L.pair_w);
+    out->pair_send = ws_ptr<int32_t>(ctx, ctx->L.pair_send);
+    out->recv_eloc = ws_ptr<int32_t>(ctx, ctx->L.recv_eloc);
+    out->recv_w = ws_ptr<float>(ctx, ctx->L.recv_w);
+    out->recv_row = ws_ptr<int32_t>(ctx, ctx->L.recv_row);
+    const bool sb = ctx->cfg.flags & EP_FLAG_SENDBUF;
+    out->send_x = sb ? ws_ptr<void>(ctx, ctx->L.send_x) : nullptr;
+    out->recv_x = sb ? ws_ptr<void>(ctx, ctx->L.recv_x) : nullptr;
+    out->slots_per_token = ctx->L.S;
+    out->expert_cap = ctx->L.Ecap;
+    out->row_bytes = (int32_t)ctx->L.row_bytes;
+    out->reserved = 0;
+    return EP_OK;
+}
+
+int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const int32_t *topk_ids,
+                const float *topk_weights, const void *const *extra_in, void *b_a1,
+                void *const *extra_out, int32_t *expert_num_tokens, int32_t path, void *stream) {
+    if (!ctx || !a1 || !topk_ids || !topk_weights || !b_a1 || !expert_num_tokens)
+        return EP_ERR_INVALID_ARG;
+    const ep_config_t &cf = ctx->cfg;
+    if (path != EP_PATH_FUSED && path != EP_PATH_SENDBUF) return EP_ERR_INVALID_ARG;
+    if (path == EP_PATH_SENDBUF && !(cf.flags & EP_FLAG_SENDBUF)) return EP_ERR_WORKSPACE;
+    if (!aligned(a1, 16) || !aligned(b_a1, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_weights, 4) || !aligned(expert_num_tokens, 4) ||
+        (num_tokens && !aligned(num_tokens, 4)))
+        return EP_ERR_INVALID_ARG;
+    if (cf.n_extra > 0) {
+        if (!extra_in || !extra_out) return EP_ERR_INVALID_ARG;
+        for (int i = 0; i < cf.n_extra; ++i)
+            if (!extra_in[i] || !extra_out[i] || !aligned(extra_in[i], 16) || !aligned(extra_out[i], 16))
+                return EP_ERR_INVALID_ARG;
+    }
+    if (ctx->state != kIdle) return EP_ERR_STATE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = lazy_init(ctx, st);
+    if (rc != EP_OK) return rc;
+
+    ctx->epoch = (ctx->epoch + 1) & 0x3FFFFFFFu;
+    if (ctx->epoch == 0) {   // wrapped: old flags could look current, clear them
+        if (cudaMemsetAsync(ctx->ws + ctx->L.tile_flag, 0, (size_t)ctx->L.num_tiles * 4, st) !=
+            cudaSuccess)
+            return EP_ERR_CUDA;
+        ctx->epoch = 1;
+    }
+    const Layout &L = ctx->L;
+    ep::RouteParams rp;
+    std::memset(&rp, 0, sizeof(rp));
+    rp.ids = topk_ids;
+    rp.weights = topk_weights;
+    rp.num_tokens = num_tokens;
+    rp.W = cf.W;
+    rp.E = cf.E;
+    rp.K = cf.top_k;
+    rp.Tm = cf.max_tokens;
+    rp.e_local = L.e_local;
+    rp.S = L.S;
+    rp.Ecap = L.Ecap;
+    rp.tiles_per_rank = L.tiles_per_rank;
+    rp.num_tiles = L.num_tiles;
+    rp.n_ctr = L.n_ctr;
+    rp.epoch = ctx->epoch;
+    rp.hdr = ws_ptr<ep::DevHeader>(ctx, L.hdr);
+    rp.tile_flag = ws_ptr<uint32_t>(ctx, L.tile_flag);
+    rp.tile_agg = ws_ptr<int32_t>(ctx, L.tile_agg);
+    rp.tile_incl = ws_ptr<int32_t>(ctx, L.tile_incl);
+    rp.send_cnt = ws_ptr<int32_t>(ctx, L.send_cnt);
+    rp.pair_row = ws_ptr<int32_t>(ctx, L.pair_row);
+    rp.pair_w = ws_ptr<float>(ctx, L.pair_w);
+    rp.pair_send = ws_ptr<int32_t>(ctx, L.pair_send);
+    rp.recv_eloc = ws_ptr<int32_t>(ctx, L.recv_eloc);
+    rp.recv_w = ws_ptr<float>(ctx, L.recv_w);
+    rp.recv_row = ws_ptr<int32_t>(ctx, L.recv_row);
+    rp.expert_num_tokens = expert_num_tokens;
+    rp.wait_limit_ns = ctx->wait_limit_ns;
+    rp.fault_skip_tile = ctx->fault_skip;
+    {
+        KernelTimer tm(ctx, EP_K_ROUTE, st);
+        if (ep::launch_route(rp, ep::route_smem_bytes(L.n_ctr), st) != cudaSuccess) return EP_ERR_CUDA;
+    }
+    const bool pdl = ctx->pdl != 0;
+    if (path == EP_PATH_FUSED) {
+        rc = launch_move_mode(ctx, ep::MOVE_FUSED, EP_K_MOVE_FUSED, a1, extra_in, b_a1, extra_out, pdl, st);
+        if (rc != EP_OK) return rc;
+    } else {
+        rc = launch_move_mode(ctx, ep::MOVE_PACK, EP_K_PACK, a1, extra_in, b_a1, extra_out, pdl, st);
+        if (rc == EP_OK)
+            rc = launch_move_mode(ctx, ep::MOVE_EXCHANGE, EP_K_EXCHANGE, a1, extra_in, b_a1, extra_out,
+                                  pdl, st);
+        if (rc == EP_OK)
+            rc = launch_move_mode(ctx, ep::MOVE_DELIVER, EP_K_DELIVER, a1, extra_in, b_a1, extra_out,
+                                  pdl, st);
+        if (rc != EP_OK) return rc;
+    }
+    if (cf.flags & EP_FLAG_ZERO_PAD) {
+        ep::ZeroPadParams zp;
+        std::memset(&zp, 0, sizeof(zp));
+        zp.n_seg = 1 + cf.n_extra;
+        zp.seg_bytes[0] = 2u * (uint32_t)cf.hidden;
+        zp.dst_seg[0] = static_cast<uint8_t *>(b_a1);
+        for (int i = 0; i < cf.n_extra; ++i) {
+            zp.seg_bytes[1 + i] = (uint32_t)cf.extra_row_bytes[i];
+            zp.dst_seg[1 + i] = static_cast<uint8_t *>(extra_out[i]);
+        }
+        zp.expert_num_tokens = expert_num_tokens;
+        zp.E = cf.E;
+        zp.Ecap = L.Ecap;
+        KernelTimer tm(ctx, EP_K_ZERO_PAD, st);
+        if (ep::launch_zero_pad(zp, 32, st) != cudaSuccess) return EP_ERR_CUDA;
+    }
+    ctx->state = kDispatched;
+    return EP_OK;
+}
+
+int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *out, void *stream) {
+    if (!ctx || !expert_out || !out) return EP_ERR_INVALID_ARG;
+    if (out_dtype != EP_BF16 && out_dtype != EP_F32) return EP_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16)) return EP_ERR_INVALID_ARG;
+    if (ctx->state != kDispatched) return EP_ERR_STATE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ep_config_t &cf = ctx->cfg;
+    ep::CombineParams cp;
+    cp.expert_out = static_cast<const uint8_t *>(expert_out);
+    cp.pair_row = ws_ptr<int32_t>(ctx, ctx->L.pair_row);
+    cp.pair_w = ws_ptr<float>(ctx, ctx->L.pair_w);
+    cp.out = out;
+    cp.K = cf.top_k;
+    cp.h = cf.hidden;
+    cp.n_tokens = cf.W * cf.max_tokens;
+    cp.nvec = cf.hidden / 8;
+    cp.n_rows = cf.E * ctx->L.Ecap;
+    const long long total = (long long)cp.n_tokens * cp.nvec;
+    long long grid = (total + 255) / 256;
+    const long long cap = (long long)ctx->num_sms * ctx->combine_ctas_per_sm;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    {
+        KernelTimer tm(ctx, EP_K_COMBINE, st);
+        if (ep::launch_combine(cp, out_dtype == EP_F32, (int)grid, ctx->pdl && !ctx->timing, st) !=
+            cudaSuccess)
+            return EP_ERR_CUDA;
+    }
+    ctx->state = kIdle;
+    return EP_OK;
+}
+
+int ep_status(ep_ctx_t *ctx, void *stream) {
+    if (!ctx) return EP_ERR_INVALID_ARG;
+    if (!ctx->initialized) return EP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
+    ep::DevHeader h;
+    if (cudaMemcpy(&h, ctx->ws + ctx->L.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return EP_ERR_CUDA;
+    if (h.err != 0 || h.err_count != 0 || h.ticket != 0 || h.done != 0) {
+        if (cudaMemset(ctx->ws + ctx->L.hdr, 0, sizeof(h)) != cudaSuccess) return EP_ERR_CUDA;
+    }
+    if (h.err != 0) return h.err;
+    if (h.ticket != 0 || h.done != 0) return EP_ERR_STATE;
+    return EP_OK;
+}
+
+int ep_kernel_times(ep_ctx_t *ctx, ep_kernel_times_t *out) {
+    if (!ctx || !out) return EP_ERR_INVALID_ARG;
+    int rc = EP_OK;
+    for (int k = 0; k < EP_K_COUNT; ++k) {
+        out->launches[k] = ctx->launches[k];
+        ctx->launches[k] = 0;
+        double tot = 0.0;
+        int64_t n = 0;
+        for (auto &pr : ctx->pending[k]) {
+            float ms = 0.f;
+            if (cudaEventSynchronize(pr.second) == cudaSuccess &&
+                cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) {
+                tot += ms;
+                ++n;
+            } else {
+                rc = EP_ERR_CUDA;
+            }
+            ctx->pool.push_back(pr.first);
+            ctx->pool.push_back(pr.second);
+        }
+        ctx->pending[k].clear();
+        out->total_ms[k] = tot;
+        out->timed[k] = n;
+    }
+    return rc;
+}
+
+}  // extern "C"

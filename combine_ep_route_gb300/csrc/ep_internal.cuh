@@ -1,0 +1,225 @@
+// ep_internal.cuh -- shared definitions of the EP dispatch/combine library:
+// workspace layout, kernel parameter blocks, device error reporting and the
+// inline-PTX wrappers (mbarrier, bulk async copies, acquire/release flags,
+// programmatic dependent launch) the sm_103a kernels use.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+// ----------------------------------------------------------------- constants
+constexpr int kRouteTile = 256;                 // tokens per routing tile = threads per CTA
+constexpr int kRouteWarps = kRouteTile / 32;
+constexpr int kAlign = 256;                     // workspace sub-buffer alignment
+constexpr int kMaxDst = EP_MAX_TOPK;            // destinations of one row, at most
+constexpr int kMaxSeg = 1 + EP_MAX_EXTRA;       // a1 + extra payloads
+constexpr uint32_t kMoveSmemBudget = 200 * 1024;  // stage memory of one mover CTA
+
+// Device-side status block at the start of the workspace.
+struct DevHeader {
+    int32_t err;          // first EP_ERR_* raised on the device, 0 if none
+    uint32_t err_count;   // how many raises since the last ep_status
+    uint32_t ticket;      // routing tiles started in this launch (reset by the last tile)
+    uint32_t done;        // routing tiles finished in this launch
+    uint32_t pad[60];
+};
+static_assert(sizeof(DevHeader) == 256, "header is one aligned block");
+
+// Byte offsets of the workspace sub-buffers.
+struct Layout {
+    size_t hdr, tile_flag, tile_agg, tile_incl, send_cnt, pair_row, pair_w, pair_send,
+        recv_eloc, recv_w, recv_row, send_x, recv_x, total;
+    int num_tiles, tiles_per_rank, n_ctr, S, Ecap, e_local;
+    uint32_t row_bytes;   // a1 row + extra rows, one send-buffer row
+};
+
+// ------------------------------------------------------------ parameter blocks
+struct RouteParams {
+    const int32_t *ids;
+    const float *weights;
+    const int32_t *num_tokens;   // may be null
+    int W, E, K, Tm, e_local, S, Ecap, tiles_per_rank, num_tiles, n_ctr;
+    uint32_t epoch;
+    DevHeader *hdr;
+    uint32_t *tile_flag;
+    int32_t *tile_agg, *tile_incl;
+    int32_t *send_cnt, *pair_row, *pair_send, *recv_eloc, *recv_row;
+    float *pair_w, *recv_w;
+    int32_t *expert_num_tokens;
+    uint64_t wait_limit_ns;
+    int32_t fault_skip_tile;
+};
+
+enum MoveMode { MOVE_FUSED = 0, MOVE_PACK = 1, MOVE_EXCHANGE = 2, MOVE_DELIVER = 3 };
+
+struct MoveParams {
+    int W, K, Tm, S, e_local, Ecap;
+    int n_seg;                          // 1 + n_extra
+    uint32_t seg_bytes[kMaxSeg];        // bytes of each payload segment
+    uint32_t seg_off[kMaxSeg];          // offset of each segment in a combined row
+    uint32_t row_bytes;                 // combined row (sum of segments)
+    const uint8_t *src_seg[kMaxSeg];    // token-major sources [W*Tm][seg_bytes]
+    uint8_t *dst_seg[kMaxSeg];          // expert-major outputs [E*Ecap][seg_bytes]
+    uint8_t *send_x, *recv_x;           // [W*W*Tm][row_bytes]
+    const int32_t *pair_row, *pair_send, *send_cnt, *recv_eloc, *recv_row;
+    int n_tokens;                       // W*Tm
+    int n_rows;                         // E*Ecap rows of the batched layout
+    int n_slots;                        // W*W*Tm send-buffer rows
+    int stages;                         // stages per pipeline
+    uint32_t stage_bytes;
+    DevHeader *hdr;
+    uint64_t wait_limit_ns;
+};
+
+struct CombineParams {
+    const uint8_t *expert_out;   // [E*Ecap][h] bf16
+    const int32_t *pair_row;
+    const float *pair_w;
+    void *out;
+    int K, h, n_tokens;
+    int n_rows;                  // E*Ecap: pair rows at or past it are never read
+    int nvec;                    // h / 8
+};
+
+struct ZeroPadParams {
+    int n_seg;
+    uint32_t seg_bytes[kMaxSeg];
+    uint8_t *dst_seg[kMaxSeg];
+    const int32_t *expert_num_tokens;   // [E]
+    int E, Ecap;
+};
+
+// --------------------------------------------------------------- device utils
+__device__ __forceinline__ void raise_error(DevHeader *hdr, int32_t code) {
+    atomicCAS(&hdr->err, 0, code);
+    atomicAdd(&hdr->err_count, 1u);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue / wait until the previous kernel's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------ mbarrier + bulk async copies
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false (and an EP_ERR_TIMEOUT raise) if the
+// limit runs out first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                  DevHeader *hdr) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) {
+            raise_error(hdr, EP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// global -> shared bulk copy completing on an mbarrier (bytes % 16 == 0, both
+// addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// shared -> global bulk copy tracked by the bulk async-group of this thread.
+__device__ __forceinline__ void bulk_s2g(void *gmem_dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(gmem_dst), "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk groups have completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ------------------------------------------------------------- kernel launchers
+// Each returns the cudaError_t of the launch.
+cudaError_t launch_route(const RouteParams &p, size_t smem, cudaStream_t st);
+size_t route_smem_bytes(int n_ctr);
+cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size_t smem, bool pdl,
+                        cudaStream_t st);
+cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
+                           cudaStream_t st);
+cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st);
+
+}  // namespace ep

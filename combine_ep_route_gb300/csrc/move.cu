@@ -1,0 +1,261 @@
+// move.cu -- the row movement of the EP dispatch, as bulk asynchronous copies.
+//
+// All four row-moving steps of `prepare` (vLLM AllToAllBatchedPrepareAndFinalize)
+// have one shape: read a row (an a1 row, possibly followed by extra payload
+// rows) once and write it to a handful of destination rows. One kernel
+// template serves them:
+//   MOVE_FUSED    a1[s][t] (+ extras)  -> b_a1[d][j][row] of every pair of t
+//                 (the direct path: no send or receive buffers)
+//   MOVE_PACK     a1[s][t] (+ extras)  -> send_x[s][d][slot] of every rank t reaches
+//   MOVE_EXCHANGE send_x[s][d][slot]   -> recv_x[d][s][slot]  (the all_to_all_single
+//                 of a multi-GPU run, here a permutation of rank blocks in HBM)
+//   MOVE_DELIVER  recv_x[d][s][slot]   -> b_a1[d][j][row] (+ extras) of every column
+//
+// Each warp of a CTA runs its own pipeline over a ring of shared-memory stages:
+// lane 0 loads a unit's row into a stage with cp.async.bulk (completion on an
+// mbarrier), then stores it to every destination with cp.async.bulk from
+// shared memory; the stage is refilled once the bulk group that read it is done.
+// The other lanes fetch the next unit's destination list while the current
+// unit's copies are in flight. Rows never pass through registers, and a row
+// with k destinations is read from HBM once.
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+// Largest b in [0, nb) with pre[b] <= u, for pre[0] = 0 <= u < pre[nb].
+__device__ __forceinline__ int find_block(const int32_t *pre, int nb, int u) {
+    int lo = 0, hi = nb;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= u) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Source row index (the whole warp gets it) and this lane's destination row
+// index (-1 for none) of unit u.
+template <int MODE>
+__device__ __forceinline__ void unit_meta(const MoveParams &p, const int32_t *pre, int u, int lane,
+                                          int &src, int &dst) {
+    dst = -1;
+    if (MODE == MOVE_FUSED || MODE == MOVE_PACK) {
+        src = u;
+        if (lane < p.K) {
+            dst = (MODE == MOVE_FUSED ? p.pair_row : p.pair_send)[(size_t)u * p.K + lane];
+            const int lim = MODE == MOVE_FUSED ? p.n_rows : p.n_slots;
+            if (dst >= lim) {   // never produced by routing; kept out of bounds checks' way
+                raise_error(p.hdr, EP_ERR_STATE);
+                dst = -1;
+            }
+        }
+    } else {
+        const int W = p.W;
+        const int b = find_block(pre, W * W, u);
+        const int slot = u - pre[b];
+        const int a = b / W, c = b - a * W;
+        if (MODE == MOVE_EXCHANGE) {   // b = (s, d): send row -> recv row
+            src = (a * W + c) * p.Tm + slot;
+            if (lane == 0) dst = (c * W + a) * p.Tm + slot;
+        } else {                       // b = (d, s): recv row -> expert rows
+            src = (a * W + c) * p.Tm + slot;
+            if (lane < p.S) {
+                const int j = p.recv_eloc[(size_t)src * p.S + lane];
+                const int r = p.recv_row[(size_t)src * p.S + lane];
+                if (j >= 0) {
+                    if (j < p.e_local && r >= 0 && r < p.Ecap) {
+                        dst = (a * p.e_local + j) * p.Ecap + r;
+                    } else {
+                        raise_error(p.hdr, EP_ERR_STATE);
+                    }
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+template <int MODE>
+__global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kStash = kMaxDst + 2;   // per stage: src, count, destinations
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int P = blockDim.x >> 5;
+    const int NS = p.stages;
+    const size_t stage_region = (size_t)P * NS * p.stage_bytes;
+    uint8_t *stages = smem + (size_t)warp * NS * p.stage_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + stage_region) + warp * NS;
+    int32_t *stash = reinterpret_cast<int32_t *>(reinterpret_cast<uint64_t *>(smem + stage_region) +
+                                                 P * NS) + warp * NS * kStash;
+    int32_t *pre = reinterpret_cast<int32_t *>(reinterpret_cast<uint64_t *>(smem + stage_region) +
+                                               P * NS) + P * NS * kStash;
+
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    // Everything below reads what the previous kernel on the stream wrote.
+    pdl_wait();
+
+    int n_units;
+    if (MODE == MOVE_EXCHANGE || MODE == MOVE_DELIVER) {
+        // exclusive prefix of the (s, d) or (d, s) slot counts, in shared memory
+        const int W = p.W, nb = W * W;
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            const int a = b / W, c = b - a * W;
+            const int n = MODE == MOVE_EXCHANGE ? p.send_cnt[b] : p.send_cnt[c * W + a];
+            pre[b] = min(max(n, 0), p.Tm);   // counts are in range; the clamp keeps it so
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int per = (nb + 31) / 32;
+            const int lo = lane * per, hi = min(nb, lo + per);
+            int sum = 0;
+            for (int b = lo; b < hi; ++b) sum += pre[b];
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            int run = incl - sum;
+            for (int b = lo; b < hi; ++b) {
+                const int v = pre[b];
+                pre[b] = run;
+                run += v;
+            }
+            if (lane == 31) pre[nb] = incl;
+        }
+        __syncthreads();
+        n_units = pre[nb];
+    } else {
+        n_units = p.n_tokens;
+        __syncwarp();
+    }
+
+    const bool src_split = MODE == MOVE_FUSED || MODE == MOVE_PACK;
+    const bool dst_split = MODE == MOVE_FUSED || MODE == MOVE_DELIVER;
+    const uint8_t *src_whole = MODE == MOVE_EXCHANGE ? p.send_x : p.recv_x;
+    uint8_t *dst_whole = MODE == MOVE_PACK ? p.send_x : p.recv_x;
+
+    const int first = blockIdx.x * P + warp, stride = gridDim.x * P;
+    const int my_n = n_units > first ? (n_units - first + stride - 1) / stride : 0;
+
+    int nxt_src = -1, nxt_dst = -1;   // metadata of the next unit to load
+    if (my_n > 0) unit_meta<MODE>(p, pre, first, lane, nxt_src, nxt_dst);
+
+    // Load unit i (the next one in order) into stage i % NS.
+    auto issue = [&](int i) {
+        const int st = i % NS;
+        int32_t *sh = stash + st * kStash;
+        const bool has = nxt_dst >= 0;
+        const uint32_t m = __ballot_sync(0xffffffffu, has);
+        if (has) sh[2 + __popc(m & lanemask_lt())] = nxt_dst;
+        const int src = nxt_src;
+        if (i + 1 < my_n) unit_meta<MODE>(p, pre, first + (i + 1) * stride, lane, nxt_src, nxt_dst);
+        if (lane == 0) {
+            sh[0] = m ? src : -1;
+            sh[1] = __popc(m);
+            uint64_t *bar = &bars[st];
+            uint8_t *stg = stages + (size_t)st * p.stage_bytes;
+            if (m) {
+                mbar_arrive_expect_tx(bar, p.row_bytes);
+                if (src_split) {
+                    for (int sg = 0; sg < p.n_seg; ++sg)
+                        bulk_g2s(stg + p.seg_off[sg], p.src_seg[sg] + (size_t)src * p.seg_bytes[sg],
+                                 p.seg_bytes[sg], bar);
+                } else {
+                    bulk_g2s(stg, src_whole + (size_t)src * p.row_bytes, p.row_bytes, bar);
+                }
+            } else {
+                mbar_arrive(bar);   // empty unit: complete the phase with no transfer
+            }
+        }
+        __syncwarp();
+    };
+
+    const int pro = my_n < NS ? my_n : NS;
+    for (int i = 0; i < pro; ++i) issue(i);
+    int consumed = 0;
+    bool ok = true;
+    for (int i = 0; i < my_n; ++i) {
+        const int st = i % NS;
+        if (lane == 0) {
+            ok = mbar_wait_bounded(&bars[st], (uint32_t)(i / NS) & 1u, p.wait_limit_ns, p.hdr);
+            const int32_t *sh = stash + st * kStash;
+            if (ok && sh[0] >= 0) {
+                const uint8_t *stg = stages + (size_t)st * p.stage_bytes;
+                const int n = sh[1];
+                for (int q = 0; q < n; ++q) {
+                    const size_t drow = (size_t)sh[2 + q];
+                    if (dst_split) {
+                        for (int sg = 0; sg < p.n_seg; ++sg)
+                            bulk_s2g(p.dst_seg[sg] + drow * p.seg_bytes[sg], stg + p.seg_off[sg],
+                                     p.seg_bytes[sg]);
+                    } else {
+                        bulk_s2g(dst_whole + drow * p.row_bytes, stg, p.row_bytes);
+                    }
+                }
+            }
+            bulk_commit();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        consumed = i + 1;
+        const int nx = i - 1 + NS;   // refill the stage unit i-1 used
+        if (i >= 1 && nx < my_n) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            issue(nx);
+        }
+    }
+    if (lane == 0) {
+        if (!ok) {
+            // drain the loads already issued before leaving (bounded)
+            // units issued so far: the prologue's, plus one refill per later iteration
+            int issued = consumed == 0 ? pro : consumed - 1 + NS;
+            if (issued > my_n) issued = my_n;
+            for (int i = consumed + 1; i < issued; ++i)
+                if (!mbar_wait_bounded(&bars[i % NS], (uint32_t)(i / NS) & 1u, p.wait_limit_ns, p.hdr))
+                    break;
+        }
+        bulk_wait_all();
+    }
+}
+
+cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size_t smem, bool pdl,
+                        cudaStream_t st) {
+    static size_t smem_set[4] = {0, 0, 0, 0};
+    const void *fn = nullptr;
+    switch (mode) {
+        case MOVE_FUSED: fn = (const void *)move_kernel<MOVE_FUSED>; break;
+        case MOVE_PACK: fn = (const void *)move_kernel<MOVE_PACK>; break;
+        case MOVE_EXCHANGE: fn = (const void *)move_kernel<MOVE_EXCHANGE>; break;
+        case MOVE_DELIVER: fn = (const void *)move_kernel<MOVE_DELIVER>; break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (smem > 48 * 1024 && smem > smem_set[mode]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set[mode] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<MoveParams *>(&p)};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace ep

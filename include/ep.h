@@ -1,0 +1,262 @@
+/*
+ * ep.h -- routed Mixture-of-Experts expert-parallel (EP) dispatch and combine
+ * on one GB300 GPU, with all W expert-parallel ranks simulated as blocks of
+ * that GPU's memory. The all-to-all exchange of a multi-GPU deployment becomes
+ * a permutation between rank blocks in HBM.
+ *
+ * What is computed follows vLLM "AllToAllBatchedPrepareAndFinalize" (page
+ * fused_moe/prepare_finalize/alltoall_batched): `capacities`, `prepare`
+ * (dispatch) and `finalize` (combine). The sizing, state rules and
+ * multi-payload dispatch follow FlashInfer "MoE All-to-All Operations
+ * (Throughput Backend)" (page flashinfer/comm/trtllm_moe_alltoall.py:
+ * `moe_a2a_get_workspace_size_per_rank`, `MoeAlltoAll.dispatch/combine`,
+ * `_A2AState`).
+ *
+ * Conventions for every entry point:
+ *   - Return value: EP_OK (0) or a negative EP_ERR_* code; nothing else.
+ *   - "device" pointers are CUDA global-memory addresses of the current device;
+ *     "host" pointers are ordinary process memory. The library never allocates
+ *     device memory: the caller owns every buffer, including the workspace,
+ *     and keeps it alive while the context uses it.
+ *   - Work is enqueued on the caller's stream (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream) with no host synchronisation, except in
+ *     ep_status and ep_kernel_times, which synchronise.
+ *   - Layouts are dense, row-major, with a leading rank dimension [W]:
+ *       a1            [W][Tm][h]            bf16
+ *       topk_ids      [W][Tm][K]            int32, negative = no expert
+ *       topk_weights  [W][Tm][K]            float32
+ *       num_tokens    [W]                   int32 (rank r holds tokens 0..num_tokens[r]-1)
+ *       b_a1          [W][e_local][Ecap][h] bf16, the batched-experts layout
+ *       expert_num_tokens [W][e_local]      int32
+ *       extra_in[i]   [W][Tm][extra_row_bytes[i]]        opaque bytes
+ *       extra_out[i]  [W][e_local][Ecap][extra_row_bytes[i]]
+ *       expert_out    like b_a1;  out  [W][Tm][h] bf16 or float32
+ *     with Tm = max_tokens, e_local = E / W, Ecap = Tm * W (rows per expert).
+ *   - Alignment: a1, b_a1, expert_out, out and every extra buffer 16 bytes;
+ *     the workspace 256 bytes; the others 4 bytes.
+ *   - A context is used by one host thread at a time. Its dispatch and combine
+ *     are ordered by the stream they are given; running one context on two
+ *     streams at once races on its workspace.
+ */
+#ifndef EP_H
+#define EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ limits */
+#define EP_MAX_W 64       /* simulated ranks */
+#define EP_MAX_E 1024     /* experts in total */
+#define EP_MAX_TOPK 16    /* experts per token */
+#define EP_MAX_EXTRA 4    /* extra payloads per dispatch */
+
+/* ------------------------------------------------------------ status codes */
+#define EP_OK 0
+#define EP_ERR_INVALID_ARG -1 /* bad config, null or misaligned pointer, bad path or dtype */
+#define EP_ERR_CAPACITY -2    /* a rank's num_tokens outside [0, max_tokens] (found on the device) */
+#define EP_ERR_STATE -3       /* dispatch twice without combine, or combine before dispatch */
+#define EP_ERR_EXPERT_ID -4   /* an expert id >= E (found on the device; the pair is dropped) */
+#define EP_ERR_DUPLICATE -5   /* an expert id repeated in one token row (found on the device;
+                                 the later occurrence is dropped) */
+#define EP_ERR_TIMEOUT -6     /* a bounded device-side wait expired; outputs of that call are invalid */
+#define EP_ERR_WORKSPACE -7   /* workspace too small or misaligned for the config or the path */
+#define EP_ERR_CUDA -8        /* a CUDA runtime call or kernel launch failed */
+
+/* ------------------------------------------------------------------- dtypes */
+#define EP_BF16 1
+#define EP_F32 2
+
+/* ----------------------------------------------------------- dispatch paths */
+#define EP_PATH_FUSED 0   /* a1 -> b_a1 directly, each token row read once */
+#define EP_PATH_SENDBUF 1 /* pack into send buffers, exchange rank blocks, deliver */
+
+/* ---------------------------------------------------------------- flags */
+#define EP_FLAG_ZERO_PAD 1u /* dispatch also zeroes b_a1 / extra_out rows at or past
+                               expert_num_tokens (the page zero-fills them); otherwise
+                               those rows are left as they were */
+#define EP_FLAG_SENDBUF 2u  /* size the workspace for EP_PATH_SENDBUF as well */
+
+typedef struct ep_config {
+    int32_t W;          /* simulated expert-parallel ranks, 1..EP_MAX_W */
+    int32_t E;          /* experts in total, a multiple of W, <= EP_MAX_E */
+    int32_t top_k;      /* experts per token, 1..min(E, EP_MAX_TOPK) */
+    int32_t max_tokens; /* token slots per rank (Tm), >= 1 */
+    int32_t hidden;     /* h, elements per a1 row; 2*h must be a multiple of 16 */
+    int32_t x_dtype;    /* EP_BF16 */
+    int32_t n_extra;    /* extra payloads, 0..EP_MAX_EXTRA */
+    int32_t extra_row_bytes[EP_MAX_EXTRA]; /* each a positive multiple of 16 */
+    uint32_t flags;     /* EP_FLAG_* */
+} ep_config_t;
+
+typedef struct ep_ctx ep_ctx_t;
+
+/*
+ * ep_capacities -- `capacities(topk)` of AllToAllBatchedPrepareAndFinalize:
+ * token slots per rank (*tok_cap = max_tokens), expert slots per token
+ * (*slots_per_token = min(top_k, e_local)) and rows per expert (*expert_cap =
+ * max_tokens * W). All pointers are host pointers. EP_ERR_INVALID_ARG for an
+ * invalid config or a null pointer. Touches no GPU.
+ */
+int ep_capacities(const ep_config_t *cfg, int32_t *tok_cap, int32_t *slots_per_token,
+                  int32_t *expert_cap);
+
+/*
+ * ep_workspace_bytes -- device workspace a context needs for cfg (host
+ * pointers in and out). Sub-buffers are padded to 256 bytes, as
+ * `moe_a2a_get_workspace_size_per_rank` pads its regions. It holds the
+ * routing metadata (`prepare`'s combine context) and, with EP_FLAG_SENDBUF, the
+ * send and receive rank blocks. Touches no GPU.
+ */
+int ep_workspace_bytes(const ep_config_t *cfg, size_t *bytes);
+
+/*
+ * ep_ctx_create -- bind a context to cfg and to a caller-owned device
+ * workspace of at least ep_workspace_bytes(cfg) bytes (256-byte aligned). The
+ * context (host memory, freed by ep_ctx_destroy) keeps pointers only. The
+ * workspace is initialised on first use, on the first dispatch's stream.
+ * Touches no GPU. EP_ERR_INVALID_ARG for a bad config or null pointer,
+ * EP_ERR_WORKSPACE for a small or misaligned workspace.
+ */
+int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_bytes,
+                  ep_ctx_t **out);
+
+/* ep_ctx_destroy -- free the host context (not the workspace). NULL is a no-op. */
+int ep_ctx_destroy(ep_ctx_t *ctx);
+
+/*
+ * ep_dispatch -- `prepare` of AllToAllBatchedPrepareAndFinalize for all W
+ * ranks at once, plus FlashInfer `MoeAlltoAll.dispatch`'s extra payloads.
+ *
+ * For every rank s and token t < num_tokens[s]: pairs with a negative id take
+ * no part; each other pair (t, k) goes to rank d = id / e_local, local expert
+ * j = id % e_local. A token goes to each rank it reaches once, in a slot
+ * numbered in token order; the slot carries the token's local ids and router
+ * weights on that rank, the k-th expert there in column k. Each rank d then
+ * writes, for sources s ascending and slots ascending, one row per column into
+ * b_a1[d][j][next free row of j], and the matching extra_out rows;
+ * expert_num_tokens[d][j] counts them. No expert can overflow Ecap.
+ *
+ *   a1, topk_ids, topk_weights : device, read-only; may be reused once the
+ *                                dispatch has run on the stream (the router
+ *                                weights are copied into the workspace).
+ *   num_tokens : device [W] or NULL (= max_tokens for every rank).
+ *   extra_in / extra_out : HOST arrays of n_extra DEVICE pointers (NULL when
+ *                          n_extra is 0).
+ *   b_a1, extra_out[i], expert_num_tokens : device, written.
+ *   path : EP_PATH_FUSED or EP_PATH_SENDBUF (needs EP_FLAG_SENDBUF).
+ *
+ * Host-side errors (returned, nothing enqueued): EP_ERR_INVALID_ARG,
+ * EP_ERR_STATE (a dispatch already awaits its combine), EP_ERR_WORKSPACE,
+ * EP_ERR_CUDA. Device-side errors (EP_ERR_EXPERT_ID, EP_ERR_DUPLICATE,
+ * EP_ERR_CAPACITY, EP_ERR_TIMEOUT) are recorded in the workspace and returned
+ * by ep_status.
+ */
+int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens,
+                const int32_t *topk_ids, const float *topk_weights,
+                const void *const *extra_in, void *b_a1, void *const *extra_out,
+                int32_t *expert_num_tokens, int32_t path, void *stream);
+
+/*
+ * ep_combine -- `finalize` of AllToAllBatchedPrepareAndFinalize for all ranks:
+ * out[s][t] = sum over the token's pairs k of w[s][t][k] * expert_out[d][j][row]
+ * of the row the pair was delivered to, folded in fp32 in top-k order (one
+ * rounded product and one rounded sum per pair) and rounded once to out_dtype
+ * (EP_BF16 nearest-even, or EP_F32). Tokens with no pair and rows at or past
+ * num_tokens[s] are written as zeros.
+ *
+ *   expert_out : device, layout of b_a1 (it may be b_a1 itself).
+ *   out        : device [W][Tm][h] of out_dtype, written.
+ *
+ * Needs a preceding ep_dispatch on this context (EP_ERR_STATE otherwise, as
+ * `MoeAlltoAll.combine` asserts); the context returns to idle afterwards.
+ */
+int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *out,
+               void *stream);
+
+/*
+ * ep_status -- synchronise the stream, then return and clear the first
+ * device-side error recorded since the last call (EP_OK if none), or
+ * EP_ERR_CUDA if the stream reports a CUDA error.
+ */
+int ep_status(ep_ctx_t *ctx, void *stream);
+
+/* ep_ctx_reset -- return the context to idle (drops a dispatch that will not be combined). */
+int ep_ctx_reset(ep_ctx_t *ctx);
+
+/*
+ * Routing metadata kept in the workspace (device pointers; valid after a
+ * dispatch has run). Filled by ep_get_metadata, which touches no GPU.
+ *   send_cnt  [W(s)][W(d)]          tokens rank s sends to rank d
+ *   pair_row  [W][Tm][K]            flat b_a1 row (d*e_local+j)*Ecap+row of each pair, -1
+ *   pair_w    [W][Tm][K]            router weight of each kept pair, 0 otherwise
+ *   pair_send [W][Tm][K]            send_x row (s*W+d)*Tm+slot for the first pair of a
+ *                                   token on each rank, -1 otherwise
+ *   recv_eloc [W(d)][W(s)][Tm][S]   local expert id per received slot and column, -1
+ *   recv_w    [W(d)][W(s)][Tm][S]   router weight per received slot and column, 0
+ *   recv_row  [W(d)][W(s)][Tm][S]   row of that column within its expert, -1
+ *   send_x / recv_x [W][W][Tm][row_bytes]  rank blocks of the send-buffer path, or NULL
+ * Entries of slots at or past send_cnt are unspecified.
+ */
+typedef struct ep_metadata {
+    int32_t *send_cnt;
+    int32_t *pair_row;
+    float *pair_w;
+    int32_t *pair_send;
+    int32_t *recv_eloc;
+    float *recv_w;
+    int32_t *recv_row;
+    void *send_x;
+    void *recv_x;
+    int32_t slots_per_token; /* S */
+    int32_t expert_cap;      /* Ecap */
+    int32_t row_bytes;       /* bytes of one send-buffer row: 2*h + sum of extra_row_bytes */
+    int32_t reserved;
+} ep_metadata_t;
+
+int ep_get_metadata(const ep_ctx_t *ctx, ep_metadata_t *out);
+
+/* ep_error_string -- static text for a status code. */
+const char *ep_error_string(int code);
+
+/* ------------------------------------------------------- tuning and checks */
+#define EP_OPT_WAIT_LIMIT_NS 1   /* bound of every device-side wait, ns (default 2e9) */
+#define EP_OPT_KERNEL_TIMING 2   /* 1: record CUDA events around every kernel */
+#define EP_OPT_PDL 3             /* 1 (default): programmatic dependent launch between kernels */
+#define EP_OPT_MOVE_CTAS_PER_SM 4 /* row-mover CTAs per SM (default 1) */
+#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 4) */
+#define EP_OPT_FAULT_SKIP_PUBLISH 6 /* test hook: the routing tile with this ticket never
+                                       publishes, so its successors' waits run out and
+                                       report EP_ERR_TIMEOUT; -1 (default) = off */
+#define EP_OPT_COMBINE_CTAS_PER_SM 7 /* combine CTAs per SM (default 8) */
+
+/* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
+int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
+
+/* Kernel kinds counted by ep_kernel_times. */
+#define EP_K_ROUTE 0
+#define EP_K_MOVE_FUSED 1
+#define EP_K_PACK 2
+#define EP_K_EXCHANGE 3
+#define EP_K_DELIVER 4
+#define EP_K_COMBINE 5
+#define EP_K_ZERO_PAD 6
+#define EP_K_COUNT 7
+
+typedef struct ep_kernel_times {
+    int64_t launches[EP_K_COUNT]; /* kernels launched, per kind, since the last read */
+    double total_ms[EP_K_COUNT];  /* summed CUDA-event durations (EP_OPT_KERNEL_TIMING on) */
+    int64_t timed[EP_K_COUNT];    /* launches those durations cover */
+} ep_kernel_times_t;
+
+/* ep_kernel_times -- read and reset the per-kernel launch counts and, with
+ * EP_OPT_KERNEL_TIMING on, the event durations (waits for the events). */
+int ep_kernel_times(ep_ctx_t *ctx, ep_kernel_times_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_H */

@@ -1,0 +1,222 @@
+"""GPU parity: the sm_103a path through the C-ABI against the CPU oracle.
+
+Dispatch outputs (expert_num_tokens, slot counts, combine map, received
+metadata, payload bytes of every delivered row) must match bit for bit;
+combine must stay within 1e-2 (bf16 out) / 1e-5 (fp32 out) max relative error
+and, since the kernel folds in the oracle's order, is also checked for
+identical bits. All five named workloads run at full size in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from combine_ep_route_gb300 import EpConfig, EpContext, EpError, workloads as wl
+from combine_ep_route_gb300 import _lib as L
+from oracle import ref
+from tests import _gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda", 0)
+
+
+def _roundtrip(x, dev, path="fused", out_f32=(False,), seed=1, ctx_kw=None, opts=None):
+    ctx = H.make_ctx(x, dev, **(ctx_kw or {}))
+    for k, v in (opts or {}).items():
+        ctx.set_option(k, v)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, path=path)
+    ctx.check()
+    m = H.oracle_meta(x)
+    assert m.err == 0
+    H.check_meta(ctx, m, x, out.expert_num_tokens)
+    H.check_rows(out, m, x, a1, extras)
+    for i, f32 in enumerate(out_f32):
+        if i:   # combine again needs a fresh dispatch (the state rule)
+            ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=path)
+            ctx.check()
+        packed = H.fill_pool_rows(out, m, x.spec.h, seed)
+        H.check_combine(ctx, out.b_a1, m, x, packed, f32)
+    return ctx, out, m
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_named_workload_full_size(dev, cfg):
+    x = wl.make(cfg)
+    _roundtrip(x, dev, out_f32=(False, True) if cfg in (1, 3) else (False,))
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_identity_experts_reproduce_a1(dev, cfg):
+    x = wl.make(cfg)
+    s = x.spec
+    ctx = H.make_ctx(x, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w, extras=extras)
+    y = ctx.combine(out.b_a1)
+    ctx.check()
+    routed = (x.topk_ids >= 0).any(axis=2)
+    got = H.bits_host(y).reshape(s.W, s.T, s.h)
+    assert np.array_equal(got[routed], x.a1[routed])
+    assert (got[~routed] == 0).all()
+
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (4, 96), (5, 40)])
+def test_sendbuf_path_matches_oracle_and_fused(dev, cfg, T):
+    x = wl.make(wl.spec(cfg, T=T) if T else wl.spec(cfg))
+    s = x.spec
+    ctx, out, m = _roundtrip(x, dev, path="sendbuf", ctx_kw=dict(sendbuf=True))
+    # send and receive rank blocks hold the oracle's packed and exchanged rows
+    md = ctx.metadata()
+    src = np.concatenate([x.a1.view(np.uint8).reshape(s.W, s.T, -1)] + x.extras, axis=2)
+    rb = src.shape[2]
+    send_x = np.zeros((s.W, s.W, s.T, rb), np.uint8)
+    ref.lib().oracle_pack(s.W, s.T, rb, m.send_cnt.ctypes.data, m.send_tok.ctypes.data,
+                          src.ctypes.data, send_x.ctypes.data)
+    recv_x = np.zeros_like(send_x)
+    ref.lib().oracle_exchange(s.W, s.T, rb, send_x.ctypes.data, recv_x.ctypes.data)
+    vs = np.arange(s.T)[None, None, :] < m.send_cnt[:, :, None]
+    vr = np.arange(s.T)[None, None, :] < m.recv_cnt[:, :, None]
+    assert np.array_equal(md["send_x"].cpu().numpy()[vs], send_x[vs])
+    assert np.array_equal(md["recv_x"].cpu().numpy()[vr], recv_x[vr])
+    # and the fused path delivers the same bytes
+    ctx2 = H.make_ctx(x, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out2 = ctx2.dispatch(a1, ids, w, num_tokens=nt, extras=extras)
+    ctx2.check()
+    H.check_rows(out2, m, x, a1, extras)
+
+
+def _custom(W, E, K, T, h, seed=0, pad=0.0, extras=(), num_tokens=None):
+    s = wl.WorkloadSpec(f"w{W}-e{E}-k{K}-t{T}-h{h}", W=W, E=E, K=K, T=T, h=h, pad_frac=pad,
+                        extra_f32_cols=tuple(extras), seed=seed)
+    return wl.make(s, num_tokens=num_tokens)
+
+
+@pytest.mark.parametrize("W,E,K,T,h,pad,extras", [
+    (1, 6, 3, 50, 64, 0.1, ()),            # one rank: a counting sort by expert
+    (4, 8, 4, 33, 32, 0.0, ()),            # K > e_local: two slots per token
+    (3, 12, 2, 300, 8, 0.2, (4,)),         # two routing tiles per rank, ragged tail, 16-B rows
+    (2, 4, 2, 1, 16, 0.0, ()),             # one token per rank
+    (64, 1024, 16, 20, 64, 0.1, (4, 12)),  # the library's limits on W, E, top_k; two extras
+    (8, 64, 8, 700, 2048, 0.05, ()),       # 3 tiles per rank
+])
+def test_edge_shapes(dev, W, E, K, T, h, pad, extras):
+    _roundtrip(_custom(W, E, K, T, h, seed=W + E + T, pad=pad, extras=extras), dev, out_f32=(False, True))
+
+
+def test_ragged_and_empty_ranks(dev):
+    nt = np.array([0, 17, 128, 3, 64, 0, 127, 1], np.int32)
+    x = _custom(8, 64, 8, 128, 256, seed=4, pad=0.05, num_tokens=nt)
+    _roundtrip(x, dev, out_f32=(False, True))
+    # every id -1: nothing is sent, nothing delivered, all outputs zero
+    x0 = _custom(4, 16, 4, 40, 64, seed=5)
+    x0.topk_ids[:] = -1
+    ctx, out, m = _roundtrip(x0, dev)
+    assert int(out.expert_num_tokens.sum()) == 0
+
+
+def test_zero_pad_flag(dev):
+    x = wl.make(wl.spec(2, T=32))
+    s = x.spec
+    ctx = H.make_ctx(x, dev, zero_pad=True)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.alloc_dispatch_outputs()
+    out.b_a1.fill_(3.0)
+    ctx.dispatch(a1, ids, w, out=out)
+    ctx.check()
+    m = H.oracle_meta(x)
+    H.check_rows(out, m, x, a1, extras)
+    b = out.b_a1.view(s.E, -1, s.h)
+    for e in range(s.E):
+        n = int(m.expert_num_tokens.reshape(-1)[e])
+        assert (b[e, n:] == 0).all()
+
+
+def test_device_errors_are_reported_and_pairs_dropped(dev):
+    x = _custom(4, 16, 4, 64, 64, seed=9)
+    x.topk_ids[0, 3, 1] = 16            # id >= E
+    x.topk_ids[2, 5, 3] = x.topk_ids[2, 5, 0]   # repeated id
+    ctx = H.make_ctx(x, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w)
+    st = ctx.status()
+    assert st in (L.EP_ERR_EXPERT_ID, L.EP_ERR_DUPLICATE)
+    m = H.oracle_meta(x)
+    assert m.err & ref.ERR_EXPERT_ID and m.err & ref.ERR_DUPLICATE
+    H.check_meta(ctx, m, x, out.expert_num_tokens)
+    H.check_rows(out, m, x, a1, extras)
+    ctx.combine(out.b_a1)
+    assert ctx.status() == 0
+    # num_tokens above max_tokens
+    bad = torch.tensor([64, 65, 0, 1], dtype=torch.int32, device=dev)
+    ctx.dispatch(a1, ids, w, num_tokens=bad)
+    assert ctx.status() == L.EP_ERR_CAPACITY
+    ctx.reset()
+
+
+def test_state_rule(dev):
+    x = wl.make(1)
+    ctx = H.make_ctx(x, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w)
+    with pytest.raises(EpError) as e:
+        ctx.dispatch(a1, ids, w)
+    assert e.value.code == L.EP_ERR_STATE
+    ctx.combine(out.b_a1)
+    with pytest.raises(EpError) as e:
+        ctx.combine(out.b_a1)
+    assert e.value.code == L.EP_ERR_STATE
+    ctx.check()
+
+
+def test_wait_limit_reports_timeout_then_recovers(dev):
+    """A routing tile that never publishes (test hook) makes its successors'
+    bounded waits run out: the call reports EP_ERR_TIMEOUT and the next
+    dispatch on the same context is correct again."""
+    x = _custom(2, 8, 2, 1024, 64, seed=3)      # 4 tiles per rank
+    ctx = H.make_ctx(x, dev)
+    ctx.set_option(L.EP_OPT_WAIT_LIMIT_NS, 20_000_000)
+    ctx.set_option(L.EP_OPT_FAULT_SKIP_PUBLISH, 2)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w)
+    assert ctx.status() == L.EP_ERR_TIMEOUT
+    ctx.reset()
+    ctx.set_option(L.EP_OPT_FAULT_SKIP_PUBLISH, -1)
+    out = ctx.dispatch(a1, ids, w)
+    ctx.check()
+    m = H.oracle_meta(x)
+    H.check_meta(ctx, m, x, out.expert_num_tokens)
+    H.check_rows(out, m, x, a1, extras)
+
+
+@pytest.mark.parametrize("opts", [
+    {L.EP_OPT_PDL: 0},
+    {L.EP_OPT_MOVE_PIPES: 1},
+    {L.EP_OPT_MOVE_PIPES: 8, L.EP_OPT_MOVE_CTAS_PER_SM: 2},
+    {L.EP_OPT_KERNEL_TIMING: 1, L.EP_OPT_COMBINE_CTAS_PER_SM: 2},
+])
+def test_launch_options_do_not_change_results(dev, opts):
+    x = wl.make(wl.spec(4, T=128))
+    _roundtrip(x, dev, opts=opts)
+
+
+def test_repeated_steps_are_identical(dev):
+    x = wl.make(wl.spec(5, T=64))
+    ctx = H.make_ctx(x, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    outs = []
+    for _ in range(4):
+        d = ctx.dispatch(a1, ids, w, num_tokens=nt)
+        outs.append((d.expert_num_tokens.clone(), ctx.combine(d.b_a1).clone()))
+    ctx.check()
+    for a, b in outs[1:]:
+        assert torch.equal(a, outs[0][0]) and torch.equal(b.view(torch.int16), outs[0][1].view(torch.int16))
