@@ -41,11 +41,17 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="fused", choices=["fused", "sendbuf"])
+    ap.add_argument("--tokens-per-rank", type=int, default=None,
+                    help="override T of the workload (a smaller case for profiling)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E of the workload (a smaller case for profiling)")
+    ap.add_argument("--hidden", type=int, default=None,
+                    help="override h of the workload (a smaller case for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -113,7 +119,7 @@ def traffic_for(kernel: str, cfg: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -128,9 +134,16 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        # start the timed region only once the sampler is producing lines
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *a):
@@ -177,6 +190,20 @@ def replica_aggregate(ms_local: float, tokens_local: int, dist=None, device=None
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
     ms, tok = float(t.item()), int(n.item())
     return ms, tok, tok / (ms * 1e-3)
+
+
+def workload_spec(args):
+    over = {}
+    if args.tokens_per_rank:
+        over["T"] = args.tokens_per_rank
+    if args.experts:
+        over["E"] = args.experts
+    if args.hidden:
+        over["h"] = args.hidden
+    s = wl.spec(args.config, **over)
+    if over:
+        s = wl.spec(args.config, name=f"{s.name}-override-T{s.T}-E{s.E}-h{s.h}", **over)
+    return s
 
 
 def dist_env():
@@ -261,7 +288,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    x = wl.make(args.config)
+    x = wl.make(workload_spec(args))
     s = x.spec
     cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(x.extra_row_bytes),
                    sendbuf=args.path == "sendbuf")
@@ -280,35 +307,45 @@ def run_ours(args):
         ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
         ctx.combine(out.b_a1, out=y)
 
-    ctx.set_option(L.EP_OPT_KERNEL_TIMING, 1)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
     ctx.check()
-    ctx.kernel_times()   # drop warm-up records
+    ctx.kernel_times()   # drop warm-up counts
 
     n = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+
+    def timed_region():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t_wall = time.perf_counter()
         for i in range(n):
-            flush.zero_()                    # L2 flush between steps (not timed)
+            flush.zero_()                    # L2 flush between steps (outside the step's events)
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
-    if world > 1:
-        dist.barrier()
-    st = ctx.status()
-    if st != 0:
-        raise SystemExit(f"device status {st} after the timed region")
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    kt = ctx.kernel_times()
+        if world > 1:
+            dist.barrier()
+        st = ctx.status()
+        if st != 0:
+            raise SystemExit(f"device status {st} after the timed region")
+        return [a.elapsed_time(b) for a, b in ev], t_wall
+
+    # 1. the headline: K steps, nothing but the library's kernels between the step events
+    with ClockSampler(local) as clk:
+        step_ms, t_wall = timed_region()
     clocks = clk.summary()
+    launches = int(sum(v[0] for v in ctx.kernel_times().values()))
+    # 2. per-kernel durations for the roofline: K more steps with CUDA events around
+    #    every kernel launch, on the launching stream
+    ctx.set_option(L.EP_OPT_KERNEL_TIMING, 1)
+    step_ms_ev, _ = timed_region()
+    kt = ctx.kernel_times()
+    ctx.set_option(L.EP_OPT_KERNEL_TIMING, 0)
     disp_b, comb_b = algorithmic_bytes(x)
     n_pairs, n_tok_routed, n_tok = workload_counts(x)
     ms, _, value = replica_aggregate(sum(step_ms) / n, n_tok, dist if world > 1 else None, dev)
@@ -323,7 +360,6 @@ def run_ours(args):
     dom_bytes = disp_b if dom == "move_fused" else comb_b
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
     traffic = traffic_for(dom, args.config)
-    launches = int(sum(v[0] for v in kt.values()))
 
     e2e = None
     if not args.no_e2e:
@@ -345,7 +381,10 @@ def run_ours(args):
         "effective_frac_of_peak": (disp_b + comb_b) / (ms * 1e-3) / 1e9 / peak,
         "alg_bytes_per_step": {"dispatch": disp_b, "combine": comb_b},
         "counts": {"pairs": n_pairs, "tokens_routed": n_tok_routed, "tokens": n_tok},
+        "pairs_per_s": world * n_pairs / (ms * 1e-3),
         "kernel_ms": {k: round(v, 5) for k, v in per.items()},
+        "kernel_ms_note": "second pass of K steps with CUDA events around every launch "
+                          f"(step {sum(step_ms_ev) / n:.4f} ms with those events)",
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic},

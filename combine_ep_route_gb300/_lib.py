@@ -43,6 +43,8 @@ EP_OPT_MOVE_CTAS_PER_SM = 4
 EP_OPT_MOVE_PIPES = 5
 EP_OPT_FAULT_SKIP_PUBLISH = 6
 EP_OPT_COMBINE_CTAS_PER_SM = 7
+EP_OPT_MOVE_CHUNK_BYTES = 8
+EP_OPT_MOVE_MAX_STAGES = 9
 
 EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD = range(7)
 EP_K_COUNT = 7

@@ -98,6 +98,8 @@ struct ep_ctx {
     int move_pipes;
     int fault_skip;
     int combine_ctas_per_sm;
+    int move_chunk_target;   // bytes; 0 = whole rows
+    int move_max_stages;
     // counters and event timing
     int64_t launches[EP_K_COUNT];
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[EP_K_COUNT];
@@ -196,8 +198,23 @@ void fill_move_common(const ep_ctx *c, ep::MoveParams &m) {
 
 // Pipelines per CTA, stages per pipeline and the dynamic shared memory of one
 // mover CTA for the current options.
+// Chunks per row: the largest count whose chunk is at least the target size
+// and a multiple of 16 bytes that divides the activation row.
+int move_chunks(const ep_ctx *c) {
+    const uint32_t a1b = 2u * (uint32_t)c->cfg.hidden;
+    if (c->move_chunk_target == 0) return 1;
+    int best = 1;
+    for (int n = 2; n <= 64; ++n) {
+        if (a1b % (16u * n) != 0) continue;
+        if (a1b / n < (uint32_t)c->move_chunk_target) break;
+        best = n;
+    }
+    return best;
+}
+
 void move_shape(const ep_ctx *c, int &pipes, int &stages, uint32_t &stage_bytes, size_t &smem) {
-    stage_bytes = (uint32_t)align_up(c->L.row_bytes, 128);
+    const uint32_t a1b = 2u * (uint32_t)c->cfg.hidden;
+    stage_bytes = (uint32_t)align_up(a1b / move_chunks(c) + (c->L.row_bytes - a1b), 128);
     const int ctas = c->move_ctas_per_sm;
     size_t budget = ctas == 1 ? ep::kMoveSmemBudget : (size_t)(220 * 1024) / ctas - 2048;
     if (budget > ep::kMoveSmemBudget) budget = ep::kMoveSmemBudget;
@@ -205,7 +222,7 @@ void move_shape(const ep_ctx *c, int &pipes, int &stages, uint32_t &stage_bytes,
     pipes = c->move_pipes;
     while (pipes > 1 && total / pipes < 2) --pipes;
     stages = total / pipes;
-    if (stages > 8) stages = 8;
+    if (stages > c->move_max_stages) stages = c->move_max_stages;
     if (stages < 2) stages = 2;
     const int W = c->cfg.W;
     smem = (size_t)pipes * stages * stage_bytes + (size_t)pipes * stages * 8 +
@@ -228,6 +245,8 @@ int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *
     move_shape(c, pipes, stages, stage_bytes, smem);
     m.stages = stages;
     m.stage_bytes = stage_bytes;
+    m.chunks = move_chunks(c);
+    m.chunk_bytes = m.seg_bytes[0] / (uint32_t)m.chunks;
     const int grid = c->num_sms * c->move_ctas_per_sm;
     KernelTimer tm(c, kind, st);
     return ep::launch_move(mode, m, grid, pipes * 32, smem, pdl && !c->timing, st) == cudaSuccess
@@ -292,11 +311,13 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->epoch = 0;
     c->wait_limit_ns = 2000000000ull;
     c->timing = 0;
-    c->pdl = 1;
+    c->pdl = 0;   // measured: the step is faster without programmatic dependent launch
     c->move_ctas_per_sm = 1;
-    c->move_pipes = 4;
+    c->move_pipes = 8;
     c->fault_skip = -1;
-    c->combine_ctas_per_sm = 8;
+    c->combine_ctas_per_sm = 0;   // 0 = as many as fit (occupancy)
+    c->move_chunk_target = 2048;
+    c->move_max_stages = 4;
     for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
     *out = c;
     return EP_OK;
@@ -348,8 +369,16 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
             ctx->fault_skip = (int)value;
             return EP_OK;
         case EP_OPT_COMBINE_CTAS_PER_SM:
-            if (value < 1 || value > 16) return EP_ERR_INVALID_ARG;
+            if (value < 0 || value > 16) return EP_ERR_INVALID_ARG;
             ctx->combine_ctas_per_sm = (int)value;
+            return EP_OK;
+        case EP_OPT_MOVE_CHUNK_BYTES:
+            if (value < 0 || value > (1 << 20) || value % 16 != 0) return EP_ERR_INVALID_ARG;
+            ctx->move_chunk_target = (int)value;
+            return EP_OK;
+        case EP_OPT_MOVE_MAX_STAGES:
+            if (value < 2 || value > 32) return EP_ERR_INVALID_ARG;
+            ctx->move_max_stages = (int)value;
             return EP_OK;
         default: return EP_ERR_INVALID_ARG;
     }
@@ -492,7 +521,10 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
     cp.n_rows = cf.E * ctx->L.Ecap;
     const long long total = (long long)cp.n_tokens * cp.nvec;
     long long grid = (total + 255) / 256;
-    const long long cap = (long long)ctx->num_sms * ctx->combine_ctas_per_sm;
+    int per_sm = ctx->combine_ctas_per_sm;
+    if (per_sm == 0 && ep::combine_occupancy(cf.top_k, out_dtype == EP_F32, &per_sm) != cudaSuccess)
+        return EP_ERR_CUDA;
+    const long long cap = (long long)ctx->num_sms * per_sm;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     {

@@ -103,13 +103,22 @@ static const void *pick_combine(bool out_f32) {
     return out_f32 ? (const void *)combine_kernel<KMAX, true> : (const void *)combine_kernel<KMAX, false>;
 }
 
+static const void *combine_fn(int K, bool out_f32) {
+    if (K <= 2) return pick_combine<2>(out_f32);
+    if (K <= 4) return pick_combine<4>(out_f32);
+    if (K <= 8) return pick_combine<8>(out_f32);
+    return pick_combine<16>(out_f32);
+}
+
+// Resident CTAs per SM of the combine kernel for this top_k (one full wave of
+// the persistent grid).
+cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, combine_fn(top_k, out_f32), 256, 0);
+}
+
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st) {
-    const void *fn;
-    if (p.K <= 2) fn = pick_combine<2>(out_f32);
-    else if (p.K <= 4) fn = pick_combine<4>(out_f32);
-    else if (p.K <= 8) fn = pick_combine<8>(out_f32);
-    else fn = pick_combine<16>(out_f32);
+    const void *fn = combine_fn(p.K, out_f32);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(256);

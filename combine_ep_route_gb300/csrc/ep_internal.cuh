@@ -63,6 +63,8 @@ struct MoveParams {
     uint32_t seg_bytes[kMaxSeg];        // bytes of each payload segment
     uint32_t seg_off[kMaxSeg];          // offset of each segment in a combined row
     uint32_t row_bytes;                 // combined row (sum of segments)
+    int chunks;                         // a1 part of a row moved as this many units
+    uint32_t chunk_bytes;               // seg_bytes[0] / chunks (multiple of 16)
     const uint8_t *src_seg[kMaxSeg];    // token-major sources [W*Tm][seg_bytes]
     uint8_t *dst_seg[kMaxSeg];          // expert-major outputs [E*Ecap][seg_bytes]
     uint8_t *send_x, *recv_x;           // [W*W*Tm][row_bytes]
@@ -220,6 +222,7 @@ cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size
                         cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st);
+cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);
 cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st);
 
 }  // namespace ep

@@ -17,7 +17,9 @@
 // shared memory; the stage is refilled once the bulk group that read it is done.
 // The other lanes fetch the next unit's destination list while the current
 // unit's copies are in flight. Rows never pass through registers, and a row
-// with k destinations is read from HBM once.
+// with k destinations is read from HBM once. A unit is one chunk of a row's
+// activation part (the extra payloads travel with chunk 0): many equal units
+// per pipeline keep the tail of the persistent grid short.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -141,11 +143,17 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
     const uint8_t *src_whole = MODE == MOVE_EXCHANGE ? p.send_x : p.recv_x;
     uint8_t *dst_whole = MODE == MOVE_PACK ? p.send_x : p.recv_x;
 
+    // units = row units x chunks, chunk-minor
+    const int C = p.chunks;
+    const uint32_t cb = p.chunk_bytes;
+    const uint32_t a1b = p.seg_bytes[0];
+    const uint32_t tail = p.row_bytes - a1b;   // extra payload bytes, moved with chunk 0
+    const int n_work = n_units * C;
     const int first = blockIdx.x * P + warp, stride = gridDim.x * P;
-    const int my_n = n_units > first ? (n_units - first + stride - 1) / stride : 0;
+    const int my_n = n_work > first ? (n_work - first + stride - 1) / stride : 0;
 
     int nxt_src = -1, nxt_dst = -1;   // metadata of the next unit to load
-    if (my_n > 0) unit_meta<MODE>(p, pre, first, lane, nxt_src, nxt_dst);
+    if (my_n > 0) unit_meta<MODE>(p, pre, first / C, lane, nxt_src, nxt_dst);
 
     // Load unit i (the next one in order) into stage i % NS.
     auto issue = [&](int i) {
@@ -155,20 +163,25 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
         const uint32_t m = __ballot_sync(0xffffffffu, has);
         if (has) sh[2 + __popc(m & lanemask_lt())] = nxt_dst;
         const int src = nxt_src;
-        if (i + 1 < my_n) unit_meta<MODE>(p, pre, first + (i + 1) * stride, lane, nxt_src, nxt_dst);
+        const int c = (first + i * stride) % C;
+        if (i + 1 < my_n) unit_meta<MODE>(p, pre, (first + (i + 1) * stride) / C, lane, nxt_src, nxt_dst);
         if (lane == 0) {
             sh[0] = m ? src : -1;
             sh[1] = __popc(m);
             uint64_t *bar = &bars[st];
             uint8_t *stg = stages + (size_t)st * p.stage_bytes;
             if (m) {
-                mbar_arrive_expect_tx(bar, p.row_bytes);
+                mbar_arrive_expect_tx(bar, cb + (c == 0 ? tail : 0u));
                 if (src_split) {
-                    for (int sg = 0; sg < p.n_seg; ++sg)
-                        bulk_g2s(stg + p.seg_off[sg], p.src_seg[sg] + (size_t)src * p.seg_bytes[sg],
-                                 p.seg_bytes[sg], bar);
+                    bulk_g2s(stg, p.src_seg[0] + (size_t)src * a1b + (size_t)c * cb, cb, bar);
+                    if (c == 0)
+                        for (int sg = 1; sg < p.n_seg; ++sg)
+                            bulk_g2s(stg + cb + (p.seg_off[sg] - a1b),
+                                     p.src_seg[sg] + (size_t)src * p.seg_bytes[sg], p.seg_bytes[sg], bar);
                 } else {
-                    bulk_g2s(stg, src_whole + (size_t)src * p.row_bytes, p.row_bytes, bar);
+                    const uint8_t *row = src_whole + (size_t)src * p.row_bytes;
+                    bulk_g2s(stg, row + (size_t)c * cb, cb, bar);
+                    if (c == 0 && tail) bulk_g2s(stg + cb, row + a1b, tail, bar);
                 }
             } else {
                 mbar_arrive(bar);   // empty unit: complete the phase with no transfer
@@ -188,15 +201,20 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
             const int32_t *sh = stash + st * kStash;
             if (ok && sh[0] >= 0) {
                 const uint8_t *stg = stages + (size_t)st * p.stage_bytes;
+                const int c = (first + i * stride) % C;
                 const int n = sh[1];
                 for (int q = 0; q < n; ++q) {
                     const size_t drow = (size_t)sh[2 + q];
                     if (dst_split) {
-                        for (int sg = 0; sg < p.n_seg; ++sg)
-                            bulk_s2g(p.dst_seg[sg] + drow * p.seg_bytes[sg], stg + p.seg_off[sg],
-                                     p.seg_bytes[sg]);
+                        bulk_s2g(p.dst_seg[0] + drow * a1b + (size_t)c * cb, stg, cb);
+                        if (c == 0)
+                            for (int sg = 1; sg < p.n_seg; ++sg)
+                                bulk_s2g(p.dst_seg[sg] + drow * p.seg_bytes[sg],
+                                         stg + cb + (p.seg_off[sg] - a1b), p.seg_bytes[sg]);
                     } else {
-                        bulk_s2g(dst_whole + drow * p.row_bytes, stg, p.row_bytes);
+                        uint8_t *row = dst_whole + drow * p.row_bytes;
+                        bulk_s2g(row + (size_t)c * cb, stg, cb);
+                        if (c == 0 && tail) bulk_s2g(row + a1b, stg + cb, tail);
                     }
                 }
             }

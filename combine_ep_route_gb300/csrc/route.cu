@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t wait_tile_flag(const uint32_t *f, uint32_t e
     uint32_t back = 32;
     for (;;) {
         __nanosleep(back);
-        if (back < 1024) back <<= 1;
+        if (back < 256) back <<= 1;
         v = ld_acquire_u32(f);
         if ((v >> 2) == epoch && (v & 3u)) return v & 3u;
         if (global_ns() - t0 > limit_ns) {
@@ -171,11 +171,13 @@ __global__ void __launch_bounds__(kRouteTile) route_kernel(const RouteParams p) 
             }
             __syncthreads();
             const int lo = s_lo, found = s_found;
+            const int rank_lo = s * p.tiles_per_rank;   // slot counters restart at each rank
             for (int c = tid; c < n_ctr; c += kRouteTile) {
-                const bool dest_ctr = c < W;   // slot counters restart at each rank
+                const int from = c < W ? max(lo, rank_lo) : lo;
                 int v = 0;
-                for (int idx = pidx; idx >= lo; --idx) {
-                    if (dest_ctr && idx / p.tiles_per_rank != s) break;
+                // independent loads (no early exit), so they are in flight together
+#pragma unroll 8
+                for (int idx = from; idx <= pidx; ++idx) {
                     const int32_t *src = (found && idx == lo) ? p.tile_incl : p.tile_agg;
                     v += __ldcg(src + (size_t)idx * vec + c);
                 }

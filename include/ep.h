@@ -225,13 +225,16 @@ const char *ep_error_string(int code);
 /* ------------------------------------------------------- tuning and checks */
 #define EP_OPT_WAIT_LIMIT_NS 1   /* bound of every device-side wait, ns (default 2e9) */
 #define EP_OPT_KERNEL_TIMING 2   /* 1: record CUDA events around every kernel */
-#define EP_OPT_PDL 3             /* 1 (default): programmatic dependent launch between kernels */
+#define EP_OPT_PDL 3             /* 1: programmatic dependent launch between kernels (default 0) */
 #define EP_OPT_MOVE_CTAS_PER_SM 4 /* row-mover CTAs per SM (default 1) */
-#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 4) */
+#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 8) */
 #define EP_OPT_FAULT_SKIP_PUBLISH 6 /* test hook: the routing tile with this ticket never
                                        publishes, so its successors' waits run out and
                                        report EP_ERR_TIMEOUT; -1 (default) = off */
-#define EP_OPT_COMBINE_CTAS_PER_SM 7 /* combine CTAs per SM (default 8) */
+#define EP_OPT_COMBINE_CTAS_PER_SM 7 /* combine CTAs per SM (default 0 = all that fit) */
+#define EP_OPT_MOVE_CHUNK_BYTES 8 /* row-mover unit: rows split into chunks of at least this
+                                     many bytes (multiple of 16; 0 = whole rows; default 2048) */
+#define EP_OPT_MOVE_MAX_STAGES 9  /* row-mover stages per pipeline, at most (2..32, default 4) */
 
 /* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
 int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);

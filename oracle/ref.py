@@ -169,6 +169,16 @@ def dispatch_rows(meta: Meta, rows: np.ndarray) -> np.ndarray:
     return out
 
 
+def _rows2d(meta: Meta, expert_rows: np.ndarray) -> np.ndarray:
+    """Packed rows as a C-contiguous [n_rows, h] uint16 array (h read from the
+    array's last axis, so an empty table keeps its width)."""
+    x = np.ascontiguousarray(expert_rows).view(np.uint16)
+    if x.ndim != 2:
+        x = x.reshape(meta.n_rows, -1)
+    assert x.shape[0] == meta.n_rows
+    return x
+
+
 def combine(meta: Meta, topk_weights: np.ndarray, expert_rows: np.ndarray, out_f32: bool = False,
             tokens: Optional[np.ndarray] = None) -> np.ndarray:
     """``finalize`` with the fixed top-k-order fp32 fold, rounded once.
@@ -180,7 +190,7 @@ def combine(meta: Meta, topk_weights: np.ndarray, expert_rows: np.ndarray, out_f
     """
     L = lib()
     W, Tm, K = meta.W, meta.Tm, meta.K
-    x = np.ascontiguousarray(expert_rows).view(np.uint16).reshape(meta.n_rows, -1)
+    x = _rows2d(meta, expert_rows)
     h = x.shape[1]
     w = np.ascontiguousarray(topk_weights, dtype=np.float32).reshape(W, Tm, K)
     out = np.zeros((W * Tm, h), np.float32 if out_f32 else np.uint16)
@@ -195,7 +205,7 @@ def combine_pagemode(meta: Meta, expert_rows: np.ndarray, out_f32: bool = False)
     """``finalize`` in the page's two-stage rounding (see ``oracle_combine_pagemode``)."""
     L = lib()
     W, Tm, K, S = meta.W, meta.Tm, meta.K, meta.S
-    x = np.ascontiguousarray(expert_rows).view(np.uint16).reshape(meta.n_rows, -1)
+    x = _rows2d(meta, expert_rows)
     h = x.shape[1]
     # flat row of each column of each send slot
     rs = np.full((W, W, Tm, S), -1, np.int32)

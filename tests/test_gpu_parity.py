@@ -203,10 +203,14 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     {L.EP_OPT_MOVE_PIPES: 1},
     {L.EP_OPT_MOVE_PIPES: 8, L.EP_OPT_MOVE_CTAS_PER_SM: 2},
     {L.EP_OPT_KERNEL_TIMING: 1, L.EP_OPT_COMBINE_CTAS_PER_SM: 2},
+    {L.EP_OPT_MOVE_CHUNK_BYTES: 2048, L.EP_OPT_MOVE_MAX_STAGES: 16},
+    {L.EP_OPT_MOVE_CHUNK_BYTES: 1024, L.EP_OPT_MOVE_MAX_STAGES: 2, L.EP_OPT_MOVE_PIPES: 2},
+    {L.EP_OPT_MOVE_CHUNK_BYTES: 0},
 ])
-def test_launch_options_do_not_change_results(dev, opts):
-    x = wl.make(wl.spec(4, T=128))
-    _roundtrip(x, dev, opts=opts)
+@pytest.mark.parametrize("path", ["fused", "sendbuf"])
+def test_launch_options_do_not_change_results(dev, opts, path):
+    x = wl.make(wl.spec(4, T=128))   # 8 KiB rows plus a 128-byte extra payload
+    _roundtrip(x, dev, opts=opts, path=path, ctx_kw=dict(sendbuf=path == "sendbuf"))
 
 
 def test_repeated_steps_are_identical(dev):
