@@ -26,6 +26,8 @@ EP_ERR_DUPLICATE = -5
 EP_ERR_TIMEOUT = -6
 EP_ERR_WORKSPACE = -7
 EP_ERR_CUDA = -8
+EP_ERR_SCRATCH_LIMIT = -9
+EP_STATIC_SCRATCH_BYTES = 4 << 20
 
 EP_BF16 = 1
 EP_F32 = 2
@@ -71,6 +73,12 @@ class EpKernelTimesC(C.Structure):
                 ("timed", C.c_int64 * EP_K_COUNT)]
 
 
+class EpRouteOutputsC(C.Structure):
+    _fields_ = [("send_cnt", C.c_void_p), ("pair_row", C.c_void_p), ("pair_w", C.c_void_p),
+                ("pair_send", C.c_void_p), ("recv_eloc", C.c_void_p), ("recv_w", C.c_void_p),
+                ("recv_row", C.c_void_p), ("expert_num_tokens", C.c_void_p), ("status", C.c_void_p)]
+
+
 # name -> (restype, argtypes); mirrors include/ep.h one to one
 SIGNATURES = {
     "ep_capacities": (C.c_int, [C.POINTER(EpConfigC), C.POINTER(C.c_int32), C.POINTER(C.c_int32),
@@ -89,6 +97,8 @@ SIGNATURES = {
     "ep_error_string": (C.c_char_p, [C.c_int]),
     "ep_set_option": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     "ep_kernel_times": (C.c_int, [C.c_void_p, C.POINTER(EpKernelTimesC)]),
+    "ep_route_static": (C.c_int, [C.POINTER(EpConfigC), C.c_void_p, C.c_void_p, C.c_void_p,
+                                  C.POINTER(EpRouteOutputsC), C.c_void_p]),
 }
 
 _lib = None

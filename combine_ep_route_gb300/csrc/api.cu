@@ -269,6 +269,7 @@ const char *ep_error_string(int code) {
         case EP_ERR_TIMEOUT: return "a bounded device wait expired";
         case EP_ERR_WORKSPACE: return "workspace too small or misaligned";
         case EP_ERR_CUDA: return "CUDA error";
+        case EP_ERR_SCRATCH_LIMIT: return "problem too large for the static scratch of ep_route_static";
         default: return "unknown status";
     }
 }

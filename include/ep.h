@@ -259,6 +259,60 @@ typedef struct ep_kernel_times {
  * EP_OPT_KERNEL_TIMING on, the event durations (waits for the events). */
 int ep_kernel_times(ep_ctx_t *ctx, ep_kernel_times_t *out);
 
+/* ------------------------------------------------- routing without allocation */
+#define EP_ERR_SCRATCH_LIMIT -9 /* the problem needs more than EP_STATIC_SCRATCH_BYTES of scratch */
+#define EP_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* Device output buffers of ep_route_static (layouts as in ep_metadata_t). */
+typedef struct ep_route_outputs {
+    int32_t *send_cnt;          /* [W(s)][W(d)] */
+    int32_t *pair_row;          /* [W][Tm][K] */
+    float *pair_w;              /* [W][Tm][K] */
+    int32_t *pair_send;         /* [W][Tm][K] */
+    int32_t *recv_eloc;         /* [W(d)][W(s)][Tm][S] */
+    float *recv_w;              /* [W(d)][W(s)][Tm][S] */
+    int32_t *recv_row;          /* [W(d)][W(s)][Tm][S] */
+    int32_t *expert_num_tokens; /* [W][e_local] */
+    int32_t *status;            /* [1] or NULL: set to 0 or to the call's first device-side
+                                   EP_ERR_* (bad id, repeated id, num_tokens out of range) */
+} ep_route_outputs_t;
+
+/*
+ * ep_route_static -- the routing step of ep_dispatch (slot and row assignment,
+ * counts, received-slot metadata) for callers that cannot allocate device
+ * memory. The pages have no counterpart: it exists for this library's users.
+ *
+ * Who needs it: code whose device memory is owned by someone else and planned
+ * up front -- an inference engine that reserves its memory pool at start-up,
+ * or a plugin whose host framework forbids allocating after initialisation --
+ * and code on a latency-critical path where a cudaMalloc (which may
+ * synchronise the device) is not acceptable. Such callers cannot create the
+ * workspace ep_ctx_create needs.
+ *
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine. Its scratch is a static device array of EP_STATIC_SCRATCH_BYTES
+ * (4 MiB) that every GPU loading this library holds until the process exits.
+ * Problems needing more scratch than that -- roughly
+ * W * ceil(max_tokens / 256) * (W + E) * 8 bytes -- are refused with
+ * EP_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *
+ * The caller passes inputs (device: num_tokens or NULL, topk_ids, topk_weights,
+ * as for ep_dispatch) and every output buffer (device, in *out). Results equal
+ * the routing metadata ep_dispatch leaves in its workspace for the same inputs.
+ *
+ * The first call on each device also performs a one-time set-up (it looks up
+ * the array's device address with that device current); make that first call
+ * before any stream capture. All calls on a device share the one array, which
+ * keeps the previous call's contents: each call clears what must start at
+ * zero on its stream. Calls that overlap on the GPU (two streams, or two host
+ * threads without ordering between their streams) race on the array.
+ *
+ * Host-side errors: EP_ERR_INVALID_ARG (bad config, null pointer),
+ * EP_ERR_SCRATCH_LIMIT, EP_ERR_CUDA. Device-side errors go to out->status.
+ */
+int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens, const int32_t *topk_ids,
+                    const float *topk_weights, const ep_route_outputs_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
