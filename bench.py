@@ -353,7 +353,7 @@ def run_ours(args):
     # per-kernel durations (CUDA events around every launch, on the launch stream)
     per = {}
     for name in ("route", "move_fused", "pack", "exchange", "deliver", "combine"):
-        launches, tot, timed = kt[name]
+        _, tot, timed = kt[name]
         if timed:
             per[name] = tot / timed
     dom = max(("move_fused", "combine"), key=lambda k: per.get(k, 0.0)) if args.path == "fused" else "combine"

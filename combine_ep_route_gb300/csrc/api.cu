@@ -37,6 +37,8 @@ bool config_ok(const ep_config_t *c) {
     const long long ecap = (long long)c->max_tokens * c->W;
     if ((long long)c->E * ecap >= (1LL << 31)) return false;
     if ((long long)c->W * c->W * c->max_tokens * c->top_k >= (1LL << 31)) return false;
+    // combine work items (token, 16-byte vector) stay within 2^31
+    if ((long long)c->W * c->max_tokens * (c->hidden / 8) >= (1LL << 31)) return false;
     return true;
 }
 
@@ -465,9 +467,11 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     rp.expert_num_tokens = expert_num_tokens;
     rp.wait_limit_ns = ctx->wait_limit_ns;
     rp.fault_skip_tile = ctx->fault_skip;
+    rp.vec_ids = aligned(topk_ids, 16) && aligned(topk_weights, 16);
+    rp.vec_recv = L.S % 4 == 0;   // workspace regions are 256-byte aligned
     {
         KernelTimer tm(ctx, EP_K_ROUTE, st);
-        if (ep::launch_route(rp, ep::route_smem_bytes(L.n_ctr), st) != cudaSuccess) return EP_ERR_CUDA;
+        if (ep::launch_route(rp, st) != cudaSuccess) return EP_ERR_CUDA;
     }
     const bool pdl = ctx->pdl != 0;
     if (path == EP_PATH_FUSED) {
@@ -519,6 +523,7 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
     cp.h = cf.hidden;
     cp.n_tokens = cf.W * cf.max_tokens;
     cp.nvec = cf.hidden / 8;
+    cp.div_nvec = ep::make_fastdiv((uint32_t)cp.nvec);
     cp.n_rows = cf.E * ctx->L.Ecap;
     const long long total = (long long)cp.n_tokens * cp.nvec;
     long long grid = (total + 255) / 256;

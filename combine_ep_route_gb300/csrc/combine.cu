@@ -50,12 +50,12 @@ template <int KMAX, bool OUT_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     pdl_wait();   // expert_out may be the previous kernel's output
     const int nvec = p.nvec, K = p.K;
-    const int64_t total = (int64_t)p.n_tokens * nvec;
+    const uint32_t total = (uint32_t)p.n_tokens * (uint32_t)nvec;   // < 2^31
     const size_t row_bytes = (size_t)p.h * 2;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int g = (int)(idx / nvec);
-        const int v = (int)(idx - (int64_t)g * nvec);
+    for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += gridDim.x * blockDim.x) {
+        const int g = (int)fastdiv(idx, p.div_nvec);
+        const int v = (int)(idx - (uint32_t)g * (uint32_t)nvec);
         int32_t r[KMAX];
         float w[KMAX];
 #pragma unroll

@@ -13,8 +13,9 @@
 namespace ep {
 
 // ----------------------------------------------------------------- constants
-constexpr int kRouteTile = 256;                 // tokens per routing tile = threads per CTA
-constexpr int kRouteWarps = kRouteTile / 32;
+constexpr int kRouteTile = 64;                  // tokens per routing tile
+constexpr int kRouteThreads = 256;              // threads per routing CTA (4 per token)
+constexpr int kRouteWarps = kRouteTile / 32;    // warps that hold one token each per lane
 constexpr int kAlign = 256;                     // workspace sub-buffer alignment
 constexpr int kMaxDst = EP_MAX_TOPK;            // destinations of one row, at most
 constexpr int kMaxSeg = 1 + EP_MAX_EXTRA;       // a1 + extra payloads
@@ -53,6 +54,8 @@ struct RouteParams {
     int32_t *expert_num_tokens;
     uint64_t wait_limit_ns;
     int32_t fault_skip_tile;
+    int32_t vec_ids;             // ids and weights 16-byte aligned: vector loads allowed
+    int32_t vec_recv;            // S % 4 == 0 and recv_* 16-byte aligned: vector row stores
 };
 
 enum MoveMode { MOVE_FUSED = 0, MOVE_PACK = 1, MOVE_EXCHANGE = 2, MOVE_DELIVER = 3 };
@@ -78,6 +81,27 @@ struct MoveParams {
     uint64_t wait_limit_ns;
 };
 
+// Division by a run-time invariant d via multiply and shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// for d >= 1 and 0 <= n < 2^31, n / d == (umulhi(n, m) + n) >> l with
+// l = ceil(log2 d) and m = floor(2^32 * (2^l - d) / d) + 1.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = (uint32_t)((((1ull << f.l) - d) << 32) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv &f) {
+    return (__umulhi(n, f.m) + n) >> f.l;
+}
+
 struct CombineParams {
     const uint8_t *expert_out;   // [E*Ecap][h] bf16
     const int32_t *pair_row;
@@ -85,7 +109,8 @@ struct CombineParams {
     void *out;
     int K, h, n_tokens;
     int n_rows;                  // E*Ecap: pair rows at or past it are never read
-    int nvec;                    // h / 8
+    int nvec;                    // h / 8; n_tokens * nvec < 2^31
+    FastDiv div_nvec;
 };
 
 struct ZeroPadParams {
@@ -216,8 +241,8 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 // ------------------------------------------------------------- kernel launchers
 // Each returns the cudaError_t of the launch.
-cudaError_t launch_route(const RouteParams &p, size_t smem, cudaStream_t st);
-size_t route_smem_bytes(int n_ctr);
+cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
+size_t route_smem_bytes(int n_ctr, int top_k);
 cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size_t smem, bool pdl,
                         cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,

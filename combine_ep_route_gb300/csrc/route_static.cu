@@ -117,7 +117,12 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     rp.expert_num_tokens = out->expert_num_tokens;
     rp.wait_limit_ns = 2000000000ull;
     rp.fault_skip_tile = -1;
-    if (ep::launch_route(rp, ep::route_smem_bytes(n_ctr), st) != cudaSuccess) return EP_ERR_CUDA;
+    rp.vec_ids = (reinterpret_cast<uintptr_t>(topk_ids) % 16 == 0) &&
+                 (reinterpret_cast<uintptr_t>(topk_weights) % 16 == 0);
+    rp.vec_recv = S % 4 == 0 && reinterpret_cast<uintptr_t>(out->recv_eloc) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(out->recv_w) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(out->recv_row) % 16 == 0;
+    if (ep::launch_route(rp, st) != cudaSuccess) return EP_ERR_CUDA;
     if (out->status) {
         static_status_kernel<<<1, 32, 0, st>>>(rp.hdr, out->status);
         if (cudaGetLastError() != cudaSuccess) return EP_ERR_CUDA;

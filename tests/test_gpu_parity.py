@@ -182,7 +182,7 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     """A routing tile that never publishes (test hook) makes its successors'
     bounded waits run out: the call reports EP_ERR_TIMEOUT and the next
     dispatch on the same context is correct again."""
-    x = _custom(2, 8, 2, 1024, 64, seed=3)      # 4 tiles per rank
+    x = _custom(2, 8, 2, 1024, 64, seed=3)      # 16 routing tiles per rank
     ctx = H.make_ctx(x, dev)
     ctx.set_option(L.EP_OPT_WAIT_LIMIT_NS, 20_000_000)
     ctx.set_option(L.EP_OPT_FAULT_SKIP_PUBLISH, 2)
