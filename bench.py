@@ -46,12 +46,17 @@ def parse():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="fused", choices=["fused", "sendbuf"])
+    ap.add_argument("--combine", default="fused", choices=["fused", "two_stage"],
+                    help="two_stage: the page's own finalize rounding (comparison only)")
     ap.add_argument("--tokens-per-rank", type=int, default=None,
                     help="override T of the workload (a smaller case for profiling)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E of the workload (a smaller case for profiling)")
     ap.add_argument("--hidden", type=int, default=None,
                     help="override h of the workload (a smaller case for profiling)")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="launch every kernel from the host each step instead of replaying one "
+                         "captured CUDA graph of dispatch + combine (the default)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -291,7 +296,7 @@ def run_ours(args):
     x = wl.make(workload_spec(args))
     s = x.spec
     cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(x.extra_row_bytes),
-                   sendbuf=args.path == "sendbuf")
+                   sendbuf=args.path == "sendbuf" or args.combine == "two_stage")
     ctx = EpContext(cfg, dev)
     a1 = torch.from_numpy(x.a1.view(np.int16)).to(dev).view(torch.bfloat16)
     ids = torch.from_numpy(x.topk_ids).to(dev)
@@ -303,15 +308,29 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    combine = ctx.combine if args.combine == "fused" else ctx.combine_two_stage
+
     def step():
         ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
-        ctx.combine(out.b_a1, out=y)
+        combine(out.b_a1, out=y)
 
-    for _ in range(max(3, args.warmup)):
+    n_warm = max(3, args.warmup)
+    for _ in range(n_warm):
         flush.zero_()
         step()
     ctx.check()
-    ctx.kernel_times()   # drop warm-up counts
+    per_step_launches = sum(v[0] for v in ctx.kernel_times().values()) // n_warm
+    eager_step = step
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            eager_step()
+        step = graph.replay
+        for _ in range(3):
+            flush.zero_()
+            step()
+        ctx.check()
+        ctx.kernel_times()
 
     n = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
@@ -340,6 +359,9 @@ def run_ours(args):
         step_ms, t_wall = timed_region()
     clocks = clk.summary()
     launches = int(sum(v[0] for v in ctx.kernel_times().values()))
+    if args.graph:   # replays do not pass through the host API: count the captured kernels
+        launches = n * per_step_launches
+    step = eager_step
     # 2. per-kernel durations for the roofline: K more steps with CUDA events around
     #    every kernel launch, on the launching stream
     ctx.set_option(L.EP_OPT_KERNEL_TIMING, 1)
@@ -352,18 +374,22 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     # per-kernel durations (CUDA events around every launch, on the launch stream)
     per = {}
-    for name in ("route", "move_fused", "pack", "exchange", "deliver", "combine"):
+    for name in ("route", "move_fused", "pack", "exchange", "deliver", "combine", "combine_two_stage"):
         _, tot, timed = kt[name]
         if timed:
             per[name] = tot / timed
-    dom = max(("move_fused", "combine"), key=lambda k: per.get(k, 0.0)) if args.path == "fused" else "combine"
-    dom_bytes = disp_b if dom == "move_fused" else comb_b
+    cands = [k for k in ("move_fused", "pack", "exchange", "deliver", "combine", "combine_two_stage")
+             if k in per]
+    dom = max(cands, key=lambda k: per[k])
+    # algorithmic bytes of one launch of the dominant kernel (send-buffer steps and the
+    # two-stage combine are charged the same algorithmic bytes as the fused step's)
+    dom_bytes = disp_b if dom in ("move_fused", "pack", "exchange", "deliver") else comb_b
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
     traffic = traffic_for(dom, args.config)
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(ctx, x, dev, out, n, stream)
+        e2e = run_e2e(ctx, x, dev, out, n, stream, combine)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.config)
@@ -374,6 +400,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": s.name, "W": s.W, "E": s.E, "top_k": s.K, "tokens_per_rank": s.T,
                    "hidden": s.h, "extra_row_bytes": list(x.extra_row_bytes), "path": args.path,
+                   "combine": args.combine, "launch": "cuda graph replay" if args.graph else "stream",
                    "out_dtype": "bf16", "accumulate": "f32", "experts": "identity (expert_out = b_a1)",
                    "l2": "flushed: 256 MiB write before every step, outside the step's events",
                    "replicas": world},
@@ -402,7 +429,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(ctx, x, dev, out, n, stream):
+def run_e2e(ctx, x, dev, out, n, stream, combine=None):
     """Same metric through the public API from pinned host buffers. Every step
     copies its own inputs host->device, dispatches, combines and copies its
     output back, all inside the timed region. Uploads and downloads run on
@@ -437,7 +464,7 @@ def run_e2e(ctx, x, dev, out, n, stream):
         stream.wait_event(out_done[b])              # step i-2's output has been read back
         a1, ids, w, *ex = d_in[b]
         ctx.dispatch(a1, ids, w, extras=ex, out=out)
-        ctx.combine(out.b_a1, out=d_y[b])
+        (combine or ctx.combine)(out.b_a1, out=d_y[b])
         comp_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])

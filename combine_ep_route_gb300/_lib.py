@@ -37,6 +37,7 @@ EP_PATH_SENDBUF = 1
 
 EP_FLAG_ZERO_PAD = 1
 EP_FLAG_SENDBUF = 2
+EP_FLAG_WEIGHT_ON_INPUT = 4
 
 EP_OPT_WAIT_LIMIT_NS = 1
 EP_OPT_KERNEL_TIMING = 2
@@ -48,9 +49,11 @@ EP_OPT_COMBINE_CTAS_PER_SM = 7
 EP_OPT_MOVE_CHUNK_BYTES = 8
 EP_OPT_MOVE_MAX_STAGES = 9
 
-EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD = range(7)
-EP_K_COUNT = 7
-KERNEL_NAMES = ("route", "move_fused", "pack", "exchange", "deliver", "combine", "zero_pad")
+(EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD,
+ EP_K_COMBINE_TWO_STAGE) = range(8)
+EP_K_COUNT = 8
+KERNEL_NAMES = ("route", "move_fused", "pack", "exchange", "deliver", "combine", "zero_pad",
+                "combine_two_stage")
 
 
 class EpConfigC(C.Structure):
@@ -91,6 +94,7 @@ SIGNATURES = {
                               C.POINTER(C.c_void_p), C.c_void_p, C.POINTER(C.c_void_p),
                               C.c_void_p, C.c_int32, C.c_void_p]),
     "ep_combine": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+    "ep_combine_two_stage": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "ep_status": (C.c_int, [C.c_void_p, C.c_void_p]),
     "ep_ctx_reset": (C.c_int, [C.c_void_p]),
     "ep_get_metadata": (C.c_int, [C.c_void_p, C.POINTER(EpMetadataC)]),

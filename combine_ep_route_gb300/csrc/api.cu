@@ -4,6 +4,7 @@
 // per-kernel event timing used by the benchmark.
 #include "ep_internal.cuh"
 
+#include <cstddef>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -30,7 +31,9 @@ bool config_ok(const ep_config_t *c) {
         if (c->extra_row_bytes[i] <= 0 || c->extra_row_bytes[i] % 16 != 0) return false;
         rb += c->extra_row_bytes[i];
     }
-    if (c->flags & ~(EP_FLAG_ZERO_PAD | EP_FLAG_SENDBUF)) return false;
+    if (c->flags & ~(EP_FLAG_ZERO_PAD | EP_FLAG_SENDBUF | EP_FLAG_WEIGHT_ON_INPUT)) return false;
+    // the page applies router weights on input for top_k == 1 only
+    if ((c->flags & EP_FLAG_WEIGHT_ON_INPUT) && c->top_k != 1) return false;
     // a row must fit twice into one mover CTA's stage memory
     if (2 * align_up((size_t)rb, 128) > ep::kMoveSmemBudget) return false;
     // flat expert row indices (E * Ecap) and flat pair indices stay within int32
@@ -91,7 +94,6 @@ struct ep_ctx {
     int state;
     bool initialized;
     int num_sms;
-    uint32_t epoch;
     // options
     uint64_t wait_limit_ns;
     int timing;
@@ -214,9 +216,10 @@ int move_chunks(const ep_ctx *c) {
     return best;
 }
 
-void move_shape(const ep_ctx *c, int &pipes, int &stages, uint32_t &stage_bytes, size_t &smem) {
+void move_shape(const ep_ctx *c, int chunks, int &pipes, int &stages, uint32_t &stage_bytes,
+                size_t &smem) {
     const uint32_t a1b = 2u * (uint32_t)c->cfg.hidden;
-    stage_bytes = (uint32_t)align_up(a1b / move_chunks(c) + (c->L.row_bytes - a1b), 128);
+    stage_bytes = (uint32_t)align_up(a1b / chunks + (c->L.row_bytes - a1b), 128);
     const int ctas = c->move_ctas_per_sm;
     size_t budget = ctas == 1 ? ep::kMoveSmemBudget : (size_t)(220 * 1024) / ctas - 2048;
     if (budget > ep::kMoveSmemBudget) budget = ep::kMoveSmemBudget;
@@ -241,13 +244,18 @@ int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *
         m.src_seg[1 + i] = static_cast<const uint8_t *>(extra_in[i]);
         m.dst_seg[1 + i] = static_cast<uint8_t *>(extra_out[i]);
     }
+    // Token-sourced steps (fused, pack) have one unit per token: rows are split
+    // into chunks so every pipeline gets many equal units. Slot-sourced steps
+    // (exchange, deliver) have one unit per sent slot, already plentiful: whole
+    // rows keep the bulk copies per byte low.
+    const int chunks = (mode == ep::MOVE_FUSED || mode == ep::MOVE_PACK) ? move_chunks(c) : 1;
     int pipes, stages;
     uint32_t stage_bytes;
     size_t smem;
-    move_shape(c, pipes, stages, stage_bytes, smem);
+    move_shape(c, chunks, pipes, stages, stage_bytes, smem);
     m.stages = stages;
     m.stage_bytes = stage_bytes;
-    m.chunks = move_chunks(c);
+    m.chunks = chunks;
     m.chunk_bytes = m.seg_bytes[0] / (uint32_t)m.chunks;
     const int grid = c->num_sms * c->move_ctas_per_sm;
     KernelTimer tm(c, kind, st);
@@ -311,7 +319,6 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->state = kIdle;
     c->initialized = false;
     c->num_sms = 0;
-    c->epoch = 0;
     c->wait_limit_ns = 2000000000ull;
     c->timing = 0;
     c->pdl = 0;   // measured: the step is faster without programmatic dependent launch
@@ -429,13 +436,6 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     int rc = lazy_init(ctx, st);
     if (rc != EP_OK) return rc;
 
-    ctx->epoch = (ctx->epoch + 1) & 0x3FFFFFFFu;
-    if (ctx->epoch == 0) {   // wrapped: old flags could look current, clear them
-        if (cudaMemsetAsync(ctx->ws + ctx->L.tile_flag, 0, (size_t)ctx->L.num_tiles * 4, st) !=
-            cudaSuccess)
-            return EP_ERR_CUDA;
-        ctx->epoch = 1;
-    }
     const Layout &L = ctx->L;
     ep::RouteParams rp;
     std::memset(&rp, 0, sizeof(rp));
@@ -452,7 +452,6 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     rp.tiles_per_rank = L.tiles_per_rank;
     rp.num_tiles = L.num_tiles;
     rp.n_ctr = L.n_ctr;
-    rp.epoch = ctx->epoch;
     rp.hdr = ws_ptr<ep::DevHeader>(ctx, L.hdr);
     rp.tile_flag = ws_ptr<uint32_t>(ctx, L.tile_flag);
     rp.tile_agg = ws_ptr<int32_t>(ctx, L.tile_agg);
@@ -469,12 +468,56 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     rp.fault_skip_tile = ctx->fault_skip;
     rp.vec_ids = aligned(topk_ids, 16) && aligned(topk_weights, 16);
     rp.vec_recv = L.S % 4 == 0;   // workspace regions are 256-byte aligned
+    rp.unit_weights = (cf.flags & EP_FLAG_WEIGHT_ON_INPUT) ? 1 : 0;
     {
         KernelTimer tm(ctx, EP_K_ROUTE, st);
         if (ep::launch_route(rp, st) != cudaSuccess) return EP_ERR_CUDA;
     }
     const bool pdl = ctx->pdl != 0;
-    if (path == EP_PATH_FUSED) {
+    if (cf.flags & EP_FLAG_WEIGHT_ON_INPUT) {
+        // rows are scaled while they move: one register-path kernel to the b_a1
+        // row (fused) or to the send row (send-buffer path, then the mover)
+        ep::ScaleMoveParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        const bool fused = path == EP_PATH_FUSED;
+        sp.a1 = static_cast<const uint8_t *>(a1);
+        sp.weights = topk_weights;
+        sp.dst_index = ws_ptr<int32_t>(ctx, fused ? L.pair_row : L.pair_send);
+        sp.n_dst_rows = fused ? cf.E * L.Ecap : cf.W * cf.W * cf.max_tokens;
+        sp.a1_bytes = 2u * (uint32_t)cf.hidden;
+        sp.nvec_a1 = sp.a1_bytes / 16;
+        sp.n_seg = 1 + cf.n_extra;
+        sp.combined = fused ? 0 : 1;
+        sp.vecs = sp.nvec_a1;
+        sp.dst[0] = fused ? static_cast<uint8_t *>(b_a1) : ws_ptr<uint8_t>(ctx, L.send_x);
+        sp.dst_stride[0] = fused ? sp.a1_bytes : L.row_bytes;
+        uint32_t off = sp.a1_bytes;
+        for (int i = 0; i < cf.n_extra; ++i) {
+            sp.src_seg[1 + i] = static_cast<const uint8_t *>(extra_in[i]);
+            sp.seg_vecs[1 + i] = (uint32_t)cf.extra_row_bytes[i] / 16;
+            sp.seg_off[1 + i] = off;
+            off += (uint32_t)cf.extra_row_bytes[i];
+            sp.dst[1 + i] = fused ? static_cast<uint8_t *>(extra_out[i]) : nullptr;
+            sp.dst_stride[1 + i] = (size_t)cf.extra_row_bytes[i];
+            sp.vecs += sp.seg_vecs[1 + i];
+        }
+        const long long items = (long long)cf.W * cf.max_tokens * sp.vecs;
+        if (items >= (1LL << 31)) return EP_ERR_INVALID_ARG;
+        sp.n_items = (uint32_t)items;
+        sp.div_vecs = ep::make_fastdiv(sp.vecs);
+        {
+            KernelTimer tm(ctx, fused ? EP_K_MOVE_FUSED : EP_K_PACK, st);
+            if (ep::launch_scale_move(sp, ctx->num_sms * 8, st) != cudaSuccess) return EP_ERR_CUDA;
+        }
+        if (!fused) {
+            rc = launch_move_mode(ctx, ep::MOVE_EXCHANGE, EP_K_EXCHANGE, a1, extra_in, b_a1, extra_out,
+                                  pdl, st);
+            if (rc == EP_OK)
+                rc = launch_move_mode(ctx, ep::MOVE_DELIVER, EP_K_DELIVER, a1, extra_in, b_a1,
+                                      extra_out, pdl, st);
+            if (rc != EP_OK) return rc;
+        }
+    } else if (path == EP_PATH_FUSED) {
         rc = launch_move_mode(ctx, ep::MOVE_FUSED, EP_K_MOVE_FUSED, a1, extra_in, b_a1, extra_out, pdl, st);
         if (rc != EP_OK) return rc;
     } else {
@@ -543,6 +586,61 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
     return EP_OK;
 }
 
+int ep_combine_two_stage(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *out,
+                         void *stream) {
+    if (!ctx || !expert_out || !out) return EP_ERR_INVALID_ARG;
+    if (out_dtype != EP_BF16 && out_dtype != EP_F32) return EP_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16)) return EP_ERR_INVALID_ARG;
+    if (!(ctx->cfg.flags & EP_FLAG_SENDBUF)) return EP_ERR_WORKSPACE;
+    if (ctx->state != kDispatched) return EP_ERR_STATE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ep_config_t &cf = ctx->cfg;
+    const Layout &L = ctx->L;
+    ep::PartialParams a;
+    a.expert_out = static_cast<const uint8_t *>(expert_out);
+    a.send_cnt = ws_ptr<int32_t>(ctx, L.send_cnt);
+    a.recv_eloc = ws_ptr<int32_t>(ctx, L.recv_eloc);
+    a.recv_row = ws_ptr<int32_t>(ctx, L.recv_row);
+    a.recv_w = ws_ptr<float>(ctx, L.recv_w);
+    a.part = ws_ptr<uint8_t>(ctx, L.recv_x);
+    a.part_stride = L.row_bytes;
+    a.W = cf.W;
+    a.Tm = cf.max_tokens;
+    a.S = L.S;
+    a.e_local = L.e_local;
+    a.Ecap = L.Ecap;
+    a.h = cf.hidden;
+    a.nvec = cf.hidden / 8;
+    a.n_items = (uint32_t)((long long)cf.W * cf.W * cf.max_tokens * a.nvec);
+    a.div_nvec = ep::make_fastdiv((uint32_t)a.nvec);
+    a.div_tm = ep::make_fastdiv((uint32_t)cf.max_tokens);
+    a.div_w = ep::make_fastdiv((uint32_t)cf.W);
+    if ((long long)cf.W * cf.W * cf.max_tokens * a.nvec >= (1LL << 31)) return EP_ERR_INVALID_ARG;
+    ep::GatherParams b;
+    b.part = a.part;
+    b.part_stride = a.part_stride;
+    b.pair_send = ws_ptr<int32_t>(ctx, L.pair_send);
+    b.out = out;
+    b.W = cf.W;
+    b.Tm = cf.max_tokens;
+    b.K = cf.top_k;
+    b.h = cf.hidden;
+    b.nvec = a.nvec;
+    b.n_items = (uint32_t)(cf.W * cf.max_tokens) * (uint32_t)b.nvec;
+    b.div_nvec = a.div_nvec;
+    b.div_tm = a.div_tm;
+    b.div_w = a.div_w;
+    const int grid = ctx->num_sms * 4;
+    {
+        KernelTimer tm(ctx, EP_K_COMBINE_TWO_STAGE, st);
+        if (ep::launch_combine_two_stage(a, b, out_dtype == EP_F32, grid, st) != cudaSuccess)
+            return EP_ERR_CUDA;
+        ctx->launches[EP_K_COMBINE_TWO_STAGE]++;   // two kernels under one timer
+    }
+    ctx->state = kIdle;
+    return EP_OK;
+}
+
 int ep_status(ep_ctx_t *ctx, void *stream) {
     if (!ctx) return EP_ERR_INVALID_ARG;
     if (!ctx->initialized) return EP_OK;
@@ -552,7 +650,10 @@ int ep_status(ep_ctx_t *ctx, void *stream) {
     if (cudaMemcpy(&h, ctx->ws + ctx->L.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
         return EP_ERR_CUDA;
     if (h.err != 0 || h.err_count != 0 || h.ticket != 0 || h.done != 0) {
-        if (cudaMemset(ctx->ws + ctx->L.hdr, 0, sizeof(h)) != cudaSuccess) return EP_ERR_CUDA;
+        // clear the error words and counters; the epoch must survive (the tile
+        // flags in the workspace carry earlier epochs)
+        if (cudaMemset(ctx->ws + ctx->L.hdr, 0, offsetof(ep::DevHeader, epoch)) != cudaSuccess)
+            return EP_ERR_CUDA;
     }
     if (h.err != 0) return h.err;
     if (h.ticket != 0 || h.done != 0) return EP_ERR_STATE;

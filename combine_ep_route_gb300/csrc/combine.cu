@@ -135,6 +135,212 @@ cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool 
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Two-stage combine: `finalize` of AllToAllBatchedPrepareAndFinalize in the
+// page's own rounding. Stage 1 runs on the receiving side of every rank: for
+// each received slot it weights the slot's columns (their expert-output rows)
+// and sums them in fp32, columns in order, then rounds the partial to bf16 --
+// the payload the page sends back with all_to_all_single. Stage 2 runs on the
+// sending side: each token sums the partials of the ranks it went to, ranks in
+// ascending order, in the output type (bf16: every sum rounded; fp32: fp32
+// sums). The exchange between the stages is no copy here: stage 2 reads the
+// other rank's block of the stage-1 buffer directly.
+template <int ST>   // slots per token rounded up to a power of two
+__global__ void __launch_bounds__(256) combine_partial_kernel(const PartialParams p) {
+    // one warp per received slot row (d, s, slot); lanes share its column list
+    const int lane = threadIdx.x & 31;
+    const uint32_t n_rows = (uint32_t)p.W * p.W * p.Tm;
+    const size_t row_bytes = (size_t)p.h * 2;
+    for (uint32_t r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n_rows;
+         r += (gridDim.x * blockDim.x) >> 5) {
+        const uint32_t ds = fastdiv(r, p.div_tm);              // d * W + s
+        const int slot = (int)(r - ds * (uint32_t)p.Tm);
+        const int d = (int)fastdiv(ds, p.div_w);
+        const int s = (int)(ds - (uint32_t)d * (uint32_t)p.W);
+        if (slot >= __ldg(p.send_cnt + s * p.W + d)) continue;   // warp-uniform
+        const size_t base = (size_t)r * p.S;
+        int64_t my_src = -1;
+        float my_w = 0.f;
+        if (lane < p.S) {
+            const int j = __ldg(p.recv_eloc + base + lane);
+            const int row = __ldg(p.recv_row + base + lane);
+            if (j >= 0 && j < p.e_local && row >= 0 && row < p.Ecap) {
+                my_src = (int64_t)(d * p.e_local + j) * p.Ecap + row;
+                my_w = __ldg(p.recv_w + base + lane);
+            }
+        }
+        // the valid columns, compacted in column order (the fold order)
+        const uint32_t vmask = __ballot_sync(0xffffffffu, my_src >= 0);
+        const int nv = __popc(vmask);
+        int64_t src[ST];
+        float w[ST];
+#pragma unroll
+        for (int c = 0; c < ST; ++c) {
+            const int from = c < nv ? __fns(vmask, 0, c + 1) : 0;
+            src[c] = __shfl_sync(0xffffffffu, my_src, from);
+            w[c] = __shfl_sync(0xffffffffu, my_w, from);
+        }
+        uint8_t *dst = p.part + (size_t)r * p.part_stride;
+        // four vectors per lane per round, so each column's loads go out together
+        for (int v0 = lane; v0 < p.nvec; v0 += 128) {
+            float a[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[u][i] = 0.f;
+            for (int c = 0; c < nv; ++c) {
+                const uint8_t *row = p.expert_out + (size_t)src[c] * row_bytes;
+                uint4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u;
+                    x[u] = v < p.nvec ? ld_stream_v4(row + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    fold2(a[u][0], a[u][1], w[c], x[u].x);
+                    fold2(a[u][2], a[u][3], w[c], x[u].y);
+                    fold2(a[u][4], a[u][5], w[c], x[u].z);
+                    fold2(a[u][6], a[u][7], w[c], x[u].w);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= p.nvec) break;
+                uint4 o;
+                o.x = pack_bf16x2(a[u][0], a[u][1]);
+                o.y = pack_bf16x2(a[u][2], a[u][3]);
+                o.z = pack_bf16x2(a[u][4], a[u][5]);
+                o.w = pack_bf16x2(a[u][6], a[u][7]);
+                *reinterpret_cast<uint4 *>(dst + (size_t)v * 16) = o;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// acc += two bf16 partials: an fp32 sum, or a bf16 sum rounded after each add.
+template <bool OUT_F32>
+__device__ __forceinline__ void add2(float &a0, float &a1, uint32_t x) {
+    const float lo = __uint_as_float(x << 16);
+    const float hi = __uint_as_float(x & 0xFFFF0000u);
+    if (OUT_F32) {
+        a0 = __fadd_rn(a0, lo);
+        a1 = __fadd_rn(a1, hi);
+    } else {
+        a0 = round_bf16(__fadd_rn(a0, lo));
+        a1 = round_bf16(__fadd_rn(a1, hi));
+    }
+}
+
+template <int KT, bool OUT_F32>
+__global__ void __launch_bounds__(256) combine_gather_kernel(const GatherParams p) {
+    // one warp per token; its destination list is read once and broadcast
+    const int lane = threadIdx.x & 31;
+    const uint32_t n_tok = (uint32_t)p.W * p.Tm;
+    for (uint32_t g = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < n_tok;
+         g += (gridDim.x * blockDim.x) >> 5) {
+        const int s = (int)fastdiv(g, p.div_tm);
+        int mine = lane < p.K ? __ldg(p.pair_send + (size_t)g * p.K + lane) : -1;
+        // the token's send rows in ascending order (= ascending destination rank)
+        int sr[KT];
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+            const int x = __shfl_sync(0xffffffffu, mine, k);
+            sr[k] = x < 0 ? 0x7FFFFFFF : x;
+        }
+#pragma unroll
+        for (int i = 1; i < KT; ++i)
+#pragma unroll
+            for (int k = i; k > 0; --k)
+                if (sr[k] < sr[k - 1]) {
+                    const int t = sr[k];
+                    sr[k] = sr[k - 1];
+                    sr[k - 1] = t;
+                }
+        int64_t rrow[KT];   // the partial row of each destination, in the rank-d block
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+            rrow[k] = -1;
+            if (sr[k] != 0x7FFFFFFF) {
+                const uint32_t sd = fastdiv((uint32_t)sr[k], p.div_tm);   // s * W + d
+                const int slot = (int)((uint32_t)sr[k] - sd * (uint32_t)p.Tm);
+                const int d = (int)(sd - (uint32_t)s * (uint32_t)p.W);
+                if (d >= 0 && d < p.W) rrow[k] = ((int64_t)d * p.W + s) * p.Tm + slot;
+            }
+        }
+        for (int v0 = lane; v0 < p.nvec; v0 += 128) {
+            float a[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[u][i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KT; ++k) {   // destinations in ascending rank order
+                if (rrow[k] < 0) continue;
+                const uint8_t *row = p.part + (size_t)rrow[k] * p.part_stride;
+                uint4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u;
+                    x[u] = v < p.nvec ? ld_stream_v4(row + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    add2<OUT_F32>(a[u][0], a[u][1], x[u].x);
+                    add2<OUT_F32>(a[u][2], a[u][3], x[u].y);
+                    add2<OUT_F32>(a[u][4], a[u][5], x[u].z);
+                    add2<OUT_F32>(a[u][6], a[u][7], x[u].w);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= p.nvec) break;
+                if (OUT_F32) {
+                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
+                                                           (size_t)v * 8);
+                    o[0] = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+                    o[1] = make_float4(a[u][4], a[u][5], a[u][6], a[u][7]);
+                } else {
+                    uint4 o;
+                    o.x = pack_bf16x2(a[u][0], a[u][1]);
+                    o.y = pack_bf16x2(a[u][2], a[u][3]);
+                    o.z = pack_bf16x2(a[u][4], a[u][5]);
+                    o.w = pack_bf16x2(a[u][6], a[u][7]);
+                    *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
+                                               (size_t)v * 16) = o;
+                }
+            }
+        }
+    }
+}
+
+template <int KT>
+static cudaError_t launch_gather_kt(const GatherParams &b, bool out_f32, int grid, cudaStream_t st) {
+    if (out_f32) combine_gather_kernel<KT, true><<<grid, 256, 0, st>>>(b);
+    else combine_gather_kernel<KT, false><<<grid, 256, 0, st>>>(b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_two_stage(const PartialParams &a, const GatherParams &b, bool out_f32,
+                                     int grid, cudaStream_t st) {
+    if (a.S <= 2) combine_partial_kernel<2><<<grid, 256, 0, st>>>(a);
+    else if (a.S <= 4) combine_partial_kernel<4><<<grid, 256, 0, st>>>(a);
+    else if (a.S <= 8) combine_partial_kernel<8><<<grid, 256, 0, st>>>(a);
+    else combine_partial_kernel<16><<<grid, 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (b.K <= 2) return launch_gather_kt<2>(b, out_f32, grid, st);
+    if (b.K <= 4) return launch_gather_kt<4>(b, out_f32, grid, st);
+    if (b.K <= 8) return launch_gather_kt<8>(b, out_f32, grid, st);
+    return launch_gather_kt<16>(b, out_f32, grid, st);
+}
+
 // Zero the rows of every expert at or past its row count, in every segment
 // (b_a1 and the extra outputs), as the page's zero-filled batched buffer.
 __global__ void __launch_bounds__(256) zero_pad_kernel(const ZeroPadParams p) {

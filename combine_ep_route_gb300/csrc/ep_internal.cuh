@@ -27,7 +27,8 @@ struct DevHeader {
     uint32_t err_count;   // how many raises since the last ep_status
     uint32_t ticket;      // routing tiles started in this launch (reset by the last tile)
     uint32_t done;        // routing tiles finished in this launch
-    uint32_t pad[60];
+    uint32_t epoch;       // look-back epoch of the running launch; the last tile advances it
+    uint32_t pad[59];
 };
 static_assert(sizeof(DevHeader) == 256, "header is one aligned block");
 
@@ -45,7 +46,6 @@ struct RouteParams {
     const float *weights;
     const int32_t *num_tokens;   // may be null
     int W, E, K, Tm, e_local, S, Ecap, tiles_per_rank, num_tiles, n_ctr;
-    uint32_t epoch;
     DevHeader *hdr;
     uint32_t *tile_flag;
     int32_t *tile_agg, *tile_incl;
@@ -56,6 +56,7 @@ struct RouteParams {
     int32_t fault_skip_tile;
     int32_t vec_ids;             // ids and weights 16-byte aligned: vector loads allowed
     int32_t vec_recv;            // S % 4 == 0 and recv_* 16-byte aligned: vector row stores
+    int32_t unit_weights;        // weights applied on input: carry 1.0 instead of w
 };
 
 enum MoveMode { MOVE_FUSED = 0, MOVE_PACK = 1, MOVE_EXCHANGE = 2, MOVE_DELIVER = 3 };
@@ -111,6 +112,50 @@ struct CombineParams {
     int n_rows;                  // E*Ecap: pair rows at or past it are never read
     int nvec;                    // h / 8; n_tokens * nvec < 2^31
     FastDiv div_nvec;
+};
+
+// Two-stage combine, stage 1: per received slot, the bf16-rounded fp32 sum of its
+// weighted columns, into part rows [W(d)][W(s)][Tm] of part_stride bytes.
+struct PartialParams {
+    const uint8_t *expert_out;      // [E*Ecap][h] bf16
+    const int32_t *send_cnt, *recv_eloc, *recv_row;
+    const float *recv_w;
+    uint8_t *part;
+    size_t part_stride;
+    int W, Tm, S, e_local, Ecap, h, nvec;
+    uint32_t n_items;               // W*W*Tm*nvec < 2^31
+    FastDiv div_nvec, div_tm, div_w;
+};
+
+// Two-stage combine, stage 2: per token, the sum over its destinations in
+// ascending order of the stage-1 rows, in the output type.
+struct GatherParams {
+    const uint8_t *part;
+    size_t part_stride;
+    const int32_t *pair_send;       // [W*Tm][K] send row (s*W+d)*Tm+slot of a token's first pair on d
+    void *out;
+    int W, Tm, K, h, nvec;
+    uint32_t n_items;               // W*Tm*nvec
+    FastDiv div_nvec, div_tm, div_w;
+};
+
+// Dispatch with apply_router_weight_on_input (top_k == 1): scaled row copies.
+struct ScaleMoveParams {
+    const uint8_t *a1;
+    const float *weights;            // [W*Tm]
+    const int32_t *dst_index;        // [W*Tm] destination row of each token's pair, -1
+    int n_dst_rows;                  // rows of the destination
+    uint32_t a1_bytes, nvec_a1;      // 2h, 2h / 16
+    int n_seg;
+    const uint8_t *src_seg[kMaxSeg];  // extras (index 1..)
+    uint32_t seg_vecs[kMaxSeg];       // 16-byte vectors of each extra row
+    uint32_t seg_off[kMaxSeg];        // byte offset of each segment in a combined row
+    uint8_t *dst[kMaxSeg];            // split: b_a1, extra_out...; combined: send_x in dst[0]
+    size_t dst_stride[kMaxSeg];
+    int combined;
+    uint32_t vecs;                    // vectors per token (a1 + extras)
+    uint32_t n_items;                 // W*Tm*vecs < 2^31
+    FastDiv div_vecs;
 };
 
 struct ZeroPadParams {
@@ -249,5 +294,8 @@ cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool 
                            cudaStream_t st);
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);
 cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st);
+cudaError_t launch_scale_move(const ScaleMoveParams &p, int grid, cudaStream_t st);
+cudaError_t launch_combine_two_stage(const PartialParams &a, const GatherParams &b, bool out_f32,
+                                     int grid, cudaStream_t st);
 
 }  // namespace ep

@@ -77,10 +77,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     int32_t *sid = agg + n_ctr;   // [64][KT] kept pair: dest << 16 | expert id; -1 if dropped
     float *sw = reinterpret_cast<float *>(sid + kRouteTile * KT);      // [64][KT]
     __shared__ int s_tile, s_lo, s_found, s_bad;
+    __shared__ uint32_t s_epoch;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         s_tile = (int)atomicAdd(&p.hdr->ticket, 1u);
+        // The epoch lives in device memory and only the launch's last tile
+        // advances it (after every tile is done), so every tile of one launch
+        // reads the same value, and a replayed launch (a CUDA graph) gets a
+        // fresh one without any host involvement.
+        s_epoch = ld_acquire_u32(&p.hdr->epoch) & 0x3FFFFFFFu;
         s_bad = 0;
     }
     for (int i = tid; i < kRouteWarps * n_ctr; i += kRouteThreads) bits[i] = 0u;
@@ -91,6 +97,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     pdl_launch_dependents();
 
     const int q = s_tile;
+    const uint32_t epoch = s_epoch;
     if (q >= p.num_tiles) {   // a stale ticket counter; never expected
         if (tid == 0) raise_error(p.hdr, EP_ERR_STATE);
         return;
@@ -180,14 +187,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
         __syncthreads();
         if (tid == 0 && publish) {
             __threadfence();
-            st_release_u32(&p.tile_flag[q], (p.epoch << 2) | 1u);
+            st_release_u32(&p.tile_flag[q], (epoch << 2) | 1u);
         }
         int pidx = q - 1;
         for (;;) {
             if (warp == 0) {
                 const int idx = pidx - lane;
                 uint32_t st = 0;
-                if (idx >= 0) st = wait_tile_flag(&p.tile_flag[idx], p.epoch, p.wait_limit_ns, p.hdr);
+                if (idx >= 0) st = wait_tile_flag(&p.tile_flag[idx], epoch, p.wait_limit_ns, p.hdr);
                 const uint32_t inc = __ballot_sync(0xffffffffu, idx >= 0 && st >= 2u);
                 if (__any_sync(0xffffffffu, st == 3u) && lane == 0) s_bad = 1;
                 if (lane == 0) {
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     __syncthreads();
     if (tid == 0 && publish) {
         __threadfence();
-        st_release_u32(&p.tile_flag[q], (p.epoch << 2) | 2u);
+        st_release_u32(&p.tile_flag[q], (epoch << 2) | 2u);
     }
 
     // 4. one thread per (token, k) pair writes the pair's row, weight and send
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
                 raise_error(p.hdr, EP_ERR_STATE);
             } else {
                 prow = e * p.Ecap + row;
-                pw = sw[tl * KT + k];
+                pw = p.unit_weights ? 1.0f : sw[tl * KT + k];
                 bool first = true;   // no earlier pair of this token on d
 #pragma unroll
                 for (int k2 = 0; k2 < KT; ++k2)
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
                         if (p2 >= 0 && (p2 >> 16) == d) {
                             const int e2 = p2 & 0xFFFF;
                             const int r2 = excl[W + e2] + wo[W + e2] + __popc(wb[W + e2] & lt);
-                            const float w2 = sw[tl * KT + k2];
+                            const float w2 = p.unit_weights ? 1.0f : sw[tl * KT + k2];
 #pragma unroll
                             for (int c = 0; c < KT; ++c)
                                 if (c == n) {
@@ -334,13 +341,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
         for (int e = tid; e < p.E; e += kRouteThreads)
             p.expert_num_tokens[e] = bad ? 0 : min(max(excl[W + e] + agg[W + e], 0), p.Ecap);
 
-    // the last tile to finish rearms the ticket for the next launch
+    // the last tile to finish rearms the ticket and advances the epoch for the
+    // next launch (every tile has published and read all it needs by now)
     __syncthreads();
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(&p.hdr->done, 1u) == (uint32_t)p.num_tiles - 1) {
             atomicExch(&p.hdr->ticket, 0u);
             atomicExch(&p.hdr->done, 0u);
+            atomicExch(&p.hdr->epoch, (epoch + 1u) & 0x3FFFFFFFu);
         }
     }
 }

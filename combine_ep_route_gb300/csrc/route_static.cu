@@ -16,6 +16,7 @@
 // through cudaGetSymbolAddress, and that address is what the kernel gets.
 #include "ep_internal.cuh"
 
+#include <cstddef>
 #include <mutex>
 
 namespace {
@@ -27,7 +28,6 @@ __device__ __align__(256) uint8_t g_route_scratch[EP_STATIC_SCRATCH_BYTES];
 
 std::mutex g_mu;
 uint8_t *g_scratch_dev[kMaxDevices];   // device address of g_route_scratch, per device
-uint32_t g_epoch[kMaxDevices];         // look-back epoch of the last call, per device
 
 size_t align_region(size_t x) { return (x + kRegionAlign - 1) / kRegionAlign * kRegionAlign; }
 
@@ -65,7 +65,6 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     if (dev < 0 || dev >= kMaxDevices) return EP_ERR_INVALID_ARG;
 
     uint8_t *scratch = nullptr;
-    uint32_t epoch = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_scratch_dev[dev]) {
@@ -75,18 +74,13 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
             g_scratch_dev[dev] = static_cast<uint8_t *>(p);
         }
         scratch = g_scratch_dev[dev];
-        epoch = (g_epoch[dev] + 1) & 0x3FFFFFFFu;
-        if (epoch == 0) {
-            // flags of a call 2^30 calls ago could look current: clear them
-            if (cudaMemsetAsync(scratch + off_flag, 0, (size_t)num_tiles * 4, st) != cudaSuccess)
-                return EP_ERR_CUDA;
-            epoch = 1;
-        }
-        g_epoch[dev] = epoch;
     }
-    // the header (first error, tile ticket, completion count) must start at zero;
-    // the array keeps whatever the previous call left in it
-    if (cudaMemsetAsync(scratch, 0, sizeof(ep::DevHeader), st) != cudaSuccess) return EP_ERR_CUDA;
+    // The header's first error, tile ticket and completion count must start at
+    // zero; the array keeps whatever the previous call left in it. Its look-back
+    // epoch is kept: the kernel advances it, so flags left by earlier calls
+    // (which carry older epochs) never look current.
+    if (cudaMemsetAsync(scratch, 0, offsetof(ep::DevHeader, epoch), st) != cudaSuccess)
+        return EP_ERR_CUDA;
 
     ep::RouteParams rp = {};
     rp.ids = topk_ids;
@@ -102,7 +96,6 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     rp.tiles_per_rank = tiles_per_rank;
     rp.num_tiles = num_tiles;
     rp.n_ctr = n_ctr;
-    rp.epoch = epoch;
     rp.hdr = reinterpret_cast<ep::DevHeader *>(scratch);
     rp.tile_flag = reinterpret_cast<uint32_t *>(scratch + off_flag);
     rp.tile_agg = reinterpret_cast<int32_t *>(scratch + off_agg);
@@ -119,6 +112,7 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     rp.fault_skip_tile = -1;
     rp.vec_ids = (reinterpret_cast<uintptr_t>(topk_ids) % 16 == 0) &&
                  (reinterpret_cast<uintptr_t>(topk_weights) % 16 == 0);
+    rp.unit_weights = (cfg->flags & EP_FLAG_WEIGHT_ON_INPUT) ? 1 : 0;
     rp.vec_recv = S % 4 == 0 && reinterpret_cast<uintptr_t>(out->recv_eloc) % 16 == 0 &&
                   reinterpret_cast<uintptr_t>(out->recv_w) % 16 == 0 &&
                   reinterpret_cast<uintptr_t>(out->recv_row) % 16 == 0;

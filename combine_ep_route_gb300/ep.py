@@ -29,6 +29,7 @@ class EpConfig:
     extra_row_bytes: Tuple[int, ...] = ()
     zero_pad: bool = False
     sendbuf: bool = False
+    weight_on_input: bool = False   # apply_router_weight_on_input (top_k == 1)
 
     @property
     def e_local(self) -> int:
@@ -41,7 +42,8 @@ class EpConfig:
         c.n_extra = len(self.extra_row_bytes)
         for i, b in enumerate(self.extra_row_bytes):
             c.extra_row_bytes[i] = int(b)
-        c.flags = (L.EP_FLAG_ZERO_PAD if self.zero_pad else 0) | (L.EP_FLAG_SENDBUF if self.sendbuf else 0)
+        c.flags = ((L.EP_FLAG_ZERO_PAD if self.zero_pad else 0) | (L.EP_FLAG_SENDBUF if self.sendbuf else 0)
+                   | (L.EP_FLAG_WEIGHT_ON_INPUT if self.weight_on_input else 0))
         return c
 
 
@@ -155,6 +157,20 @@ class EpContext:
         code = {torch.bfloat16: L.EP_BF16, torch.float32: L.EP_F32}[out_dtype]
         L.check(L.lib().ep_combine(self._h, expert_out.data_ptr(), code, out.data_ptr(),
                                    _stream_ptr(stream)), "ep_combine")
+        return out
+
+    def combine_two_stage(self, expert_out: torch.Tensor, out: Optional[torch.Tensor] = None,
+                          out_dtype: torch.dtype = torch.bfloat16,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """``finalize`` in the page's two-stage rounding (needs ``sendbuf=True``)."""
+        c, dev = self.cfg, self.device
+        _need(expert_out, "expert_out", torch.bfloat16, (c.W, c.e_local, self.expert_cap, c.hidden), dev)
+        if out is None:
+            out = torch.empty((c.W, c.max_tokens, c.hidden), dtype=out_dtype, device=dev)
+        _need(out, "out", out_dtype, (c.W, c.max_tokens, c.hidden), dev)
+        code = {torch.bfloat16: L.EP_BF16, torch.float32: L.EP_F32}[out_dtype]
+        L.check(L.lib().ep_combine_two_stage(self._h, expert_out.data_ptr(), code, out.data_ptr(),
+                                             _stream_ptr(stream)), "ep_combine_two_stage")
         return out
 
     # ---------------------------------------------------------- utilities

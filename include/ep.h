@@ -79,6 +79,9 @@ extern "C" {
                                expert_num_tokens (the page zero-fills them); otherwise
                                those rows are left as they were */
 #define EP_FLAG_SENDBUF 2u  /* size the workspace for EP_PATH_SENDBUF as well */
+#define EP_FLAG_WEIGHT_ON_INPUT 4u /* apply_router_weight_on_input of `prepare`: top_k must be
+                                      1; dispatch delivers bf16(a1 * bf16(w)) and carries unit
+                                      weights, so combine returns the expert row unweighted */
 
 typedef struct ep_config {
     int32_t W;          /* simulated expert-parallel ranks, 1..EP_MAX_W */
@@ -178,6 +181,25 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
                void *stream);
 
 /*
+ * ep_combine_two_stage -- `finalize` of AllToAllBatchedPrepareAndFinalize in
+ * the page's own two-stage rounding, for comparison with ep_combine. Stage 1,
+ * on each receiving rank d: for every received slot, sum its columns' expert
+ * rows weighted by the router weights in fp32 (columns in order) and round the
+ * partial to bf16 -- the payload the page returns with all_to_all_single.
+ * Stage 2, on each sending rank s: out[s][t] = the sum of the token's partials
+ * over the ranks it went to, ranks ascending, in out_dtype (EP_BF16: each sum
+ * rounded to bf16; EP_F32: fp32 sums). It moves about twice the bytes of
+ * ep_combine and rounds more often; results stay within the page's bound of
+ * the single fold (2^-6 * sum_k |w_k x_k| element-wise).
+ *
+ * Needs a workspace sized with EP_FLAG_SENDBUF (its receive blocks hold the
+ * stage-1 partials; EP_ERR_WORKSPACE otherwise) and a preceding ep_dispatch
+ * (EP_ERR_STATE otherwise); arguments and state rule as ep_combine.
+ */
+int ep_combine_two_stage(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *out,
+                         void *stream);
+
+/*
  * ep_status -- synchronise the stream, then return and clear the first
  * device-side error recorded since the last call (EP_OK if none), or
  * EP_ERR_CUDA if the stream reports a CUDA error.
@@ -247,7 +269,8 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
 #define EP_K_DELIVER 4
 #define EP_K_COMBINE 5
 #define EP_K_ZERO_PAD 6
-#define EP_K_COUNT 7
+#define EP_K_COMBINE_TWO_STAGE 7
+#define EP_K_COUNT 8
 
 typedef struct ep_kernel_times {
     int64_t launches[EP_K_COUNT]; /* kernels launched, per kind, since the last read */

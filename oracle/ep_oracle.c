@@ -318,6 +318,24 @@ void oracle_combine(int W, int E, int K, int Tm, int h, const int32_t *num_token
 }
 
 /*
+ * `prepare` with apply_router_weight_on_input (the page allows it for top_k == 1
+ * only): a1 is multiplied by the router weight converted to the activation
+ * type, a1 = a1 * topk_weights.to(a1.dtype), so each element becomes
+ * bf16(x * bf16(w)); the weights carried on are then all one. rows are [n][h]
+ * bf16 bits, weights [n].
+ */
+void oracle_scale_input(int64_t n, int h, const uint16_t *rows, const float *weights,
+                        uint16_t *out) {
+    for (int64_t g = 0; g < n; ++g) {
+        float w = bf16_to_f32(f32_to_bf16(weights[g]));
+        for (int i = 0; i < h; ++i) {
+            float x = bf16_to_f32(rows[g * h + i]);
+            out[g * h + i] = f32_to_bf16(x * w);
+        }
+    }
+}
+
+/*
  * `finalize` in the page's own two-stage form, kept for comparison: on each
  * rank d the pairs of each received slot are weighted and summed in fp32
  * (columns in order), the partial is rounded to bf16 (the activation type) for

@@ -42,9 +42,11 @@ def lib():
         _lib.oracle_deliver.argtypes = [i, i, i, C.c_size_t, P, P, P, P, P]
         _lib.oracle_combine.argtypes = [i, i, i, i, i, P, P, P, P, P, i, P, P, C.c_int64]
         _lib.oracle_combine_pagemode.argtypes = [i, i, i, i, i, P, P, P, P, P, P, P, i, P]
+        _lib.oracle_scale_input.argtypes = [C.c_int64, i, P, P, P]
         for f in ("oracle_capacities", "oracle_route", "oracle_exchange_meta",
                   "oracle_deliver_meta", "oracle_pair_rows", "oracle_pack", "oracle_exchange",
-                  "oracle_deliver", "oracle_combine", "oracle_combine_pagemode"):
+                  "oracle_deliver", "oracle_combine", "oracle_combine_pagemode",
+                  "oracle_scale_input"):
             getattr(_lib, f).restype = None
     return _lib
 
@@ -217,4 +219,17 @@ def combine_pagemode(meta: Meta, expert_rows: np.ndarray, out_f32: bool = False)
     L.oracle_combine_pagemode(W, meta.E, K, Tm, h, _p(meta.send_cnt), _p(meta.send_tok),
                               _p(meta.send_eloc), _p(meta.send_w), _p(rs), _p(x),
                               _p(meta.row_off), int(out_f32), _p(out))
+    return out
+
+
+def scale_input(a1: np.ndarray, topk_weights: np.ndarray) -> np.ndarray:
+    """``prepare``'s apply_router_weight_on_input (top_k == 1): a1 * bf16(w) rounded
+    to bf16, per token. a1: [..., h] bf16 bits; topk_weights: [..., 1]."""
+    x = np.ascontiguousarray(a1).view(np.uint16)
+    h = x.shape[-1]
+    n = x.size // h
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32).reshape(-1)
+    assert w.size == n, "apply_router_weight_on_input needs top_k == 1"
+    out = np.empty_like(x)
+    lib().oracle_scale_input(n, h, _p(x), _p(w), _p(out))
     return out

@@ -64,7 +64,7 @@ def test_capacities_match_oracle(lib, W, E, K, T):
 @pytest.mark.parametrize("bad", [
     dict(W=0), dict(W=65, E=1040), dict(E=60), dict(E=2048), dict(K=0), dict(K=17), dict(T=0),
     dict(h=4), dict(h=12), dict(extras=(20,)), dict(extras=(16,) * 4, n_extra=5), dict(n_extra=-1), dict(flags=8),
-    dict(h=60000), dict(W=64, E=1024, T=40000),
+    dict(h=60000), dict(W=64, E=1024, T=40000), dict(K=2, flags=4),
 ])
 def test_invalid_configs_rejected(lib, bad):
     n = C.c_size_t()
@@ -130,6 +130,17 @@ def test_host_side_argument_and_state_checks(lib):
     assert lib.ep_status(h, None) == 0
     assert lib.ep_ctx_reset(h) == 0
     assert lib.ep_ctx_destroy(h) == 0
+
+
+def test_two_stage_combine_host_checks(lib):
+    p = C.c_void_p(FAKE_WS)
+    h, _ = _ctx(lib)                                  # no send-buffer workspace
+    assert lib.ep_combine_two_stage(h, p, L.EP_BF16, p, None) == L.EP_ERR_WORKSPACE
+    lib.ep_ctx_destroy(h)
+    h, _ = _ctx(lib, cfg(flags=L.EP_FLAG_SENDBUF))
+    assert lib.ep_combine_two_stage(h, p, L.EP_BF16, p, None) == L.EP_ERR_STATE
+    assert lib.ep_combine_two_stage(h, p, 3, p, None) == L.EP_ERR_INVALID_ARG
+    lib.ep_ctx_destroy(h)
 
 
 def test_extra_payload_pointers_required(lib):

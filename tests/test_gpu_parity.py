@@ -224,3 +224,87 @@ def test_repeated_steps_are_identical(dev):
     ctx.check()
     for a, b in outs[1:]:
         assert torch.equal(a, outs[0][0]) and torch.equal(b.view(torch.int16), outs[0][1].view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (3, 128), (4, 96), (5, 40)])
+def test_two_stage_combine_matches_page_mode_oracle(dev, cfg, T):
+    """ep_combine_two_stage restates the page's own finalize (bf16 per-rank partials,
+    summed over ranks in the output type): bit-identical to the oracle's page-mode
+    combine, and within the page's bound of the single-rounding fold."""
+    x = wl.make(wl.spec(cfg, T=T) if T else wl.spec(cfg))
+    s = x.spec
+    ctx = H.make_ctx(x, dev, sendbuf=True)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    m = H.oracle_meta(x)
+    for f32 in (False, True):
+        out = ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras)
+        ctx.check()
+        packed = H.fill_pool_rows(out, m, s.h, 3)
+        got = ctx.combine_two_stage(out.b_a1, out_dtype=torch.float32 if f32 else torch.bfloat16)
+        ctx.check()
+        exp = ref.combine_pagemode(m, packed, out_f32=f32)
+        if f32:
+            g = got.cpu().numpy().reshape(-1, s.h)
+        else:
+            g = H.bits_host(got).reshape(-1, s.h)
+        assert np.array_equal(g, exp), "two-stage combine differs from the page-mode oracle"
+        single = ref.combine(m, x.topk_weights, packed, out_f32=f32)
+        gf = g if f32 else wl.bf16_bits_to_f32(g)
+        sf = single if f32 else wl.bf16_bits_to_f32(single)
+        assert np.linalg.norm(gf.astype(np.float64) - sf) <= 1e-2 * np.linalg.norm(sf)
+
+
+@pytest.mark.parametrize("path", ["fused", "sendbuf"])
+def test_weight_on_input_top1(dev, path):
+    """apply_router_weight_on_input: rows arrive as bf16(a1 * bf16(w)) and combine
+    carries unit weights (vLLM AllToAllBatchedPrepareAndFinalize.prepare)."""
+    x = _custom(8, 64, 1, 256, 2048, seed=21, pad=0.05, extras=(4,))
+    s = x.spec
+    ctx = H.make_ctx(x, dev, sendbuf=path == "sendbuf", weight_on_input=True)
+    a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+    out = ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, path=path)
+    ctx.check()
+    ones = np.ones_like(x.topk_weights)
+    m = ref.dispatch_meta(s.W, s.E, s.K, s.T, x.topk_ids, ones, x.num_tokens)
+    H.check_meta(ctx, m, wl.Workload(x.spec, x.a1, x.topk_ids, ones, x.num_tokens, x.extras),
+                 out.expert_num_tokens)
+    scaled = ref.scale_input(x.a1, x.topk_weights)
+    H.check_rows(out, m, x, H.bf16_dev(scaled, dev), extras)
+    y = ctx.combine(out.b_a1)
+    ctx.check()
+    exp = ref.combine(m, ones, ref.dispatch_rows(m, scaled))
+    assert np.array_equal(H.bits_host(y).reshape(-1, s.h), exp)
+
+
+def test_graph_replay_on_new_inputs(dev):
+    """A dispatch + combine captured once in a CUDA graph and replayed on new
+    inputs copied into the same buffers stays exact: the routing look-back epoch
+    advances on the device, so no host call is needed between replays."""
+    xs = [wl.make(wl.spec(5, T=64), seed=s) for s in (11, 12, 13)]
+    x0 = xs[0]
+    s = x0.spec
+    ctx = H.make_ctx(x0, dev)
+    a1, ids, w, nt, extras = H.inputs_dev(x0, dev)
+    out = ctx.alloc_dispatch_outputs()
+    y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
+    ctx.dispatch(a1, ids, w, num_tokens=nt, out=out)   # first use initialises the workspace
+    ctx.combine(out.b_a1, out=y)
+    ctx.check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ctx.dispatch(a1, ids, w, num_tokens=nt, out=out)
+        ctx.combine(out.b_a1, out=y)
+    for x in xs:
+        a1n, idsn, wn, ntn, _ = H.inputs_dev(x, dev)
+        a1.copy_(a1n)
+        ids.copy_(idsn)
+        w.copy_(wn)
+        nt.copy_(ntn)
+        g.replay()
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        m = H.oracle_meta(x)
+        assert np.array_equal(out.expert_num_tokens.cpu().numpy(), m.expert_num_tokens)
+        H.check_rows(out, m, x, a1, [])
+        exp = ref.combine(m, x.topk_weights, ref.dispatch_rows(m, x.a1))
+        assert np.array_equal(H.bits_host(y).reshape(-1, s.h), exp)

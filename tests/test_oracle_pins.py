@@ -385,3 +385,24 @@ def test_pagemode_two_stage_rounding_bounded():
     m = ref.dispatch_meta(s.W, s.E, s.K, s.T, ids, x.topk_weights)
     rows = _rand_expert_rows(m, s.h, 8)
     assert np.array_equal(ref.combine(m, x.topk_weights, rows), ref.combine_pagemode(m, rows))
+
+
+# ------------------------------------------- apply_router_weight_on_input
+
+def test_weight_on_input_scaling_closed_forms():
+    """prepare with apply_router_weight_on_input (top_k == 1): a1 * bf16(w), rounded
+    to bf16. Powers of two scale exactly, -1 negates, and a weight that bf16 cannot
+    hold is rounded to bf16 *before* the product (1 + 2^-10 becomes exactly 1)."""
+    rng = np.random.default_rng(5)
+    a = wl.f32_to_bf16_bits(rng.standard_normal((12, 96), dtype=np.float32))
+    x = wl.bf16_bits_to_f32(a)
+    for w, expect in [(0.5, x * 0.5), (1.0, x), (-1.0, -x), (0.125, x / 8), (4.0, x * 4),
+                      (1.0 + 2.0 ** -10, x)]:
+        got = ref.scale_input(a, np.full((12, 1), w, np.float32))
+        assert np.array_equal(wl.bf16_bits_to_f32(got), expect), w
+    # a general weight: one rounding of the exact product (bf16 x bf16 fits in fp32)
+    w = rng.random((12, 1), dtype=np.float32) + 0.1
+    wb = wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(w))
+    exact = x.astype(np.float64) * wb.astype(np.float64)
+    got = wl.bf16_bits_to_f32(ref.scale_input(a, w)).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact))
