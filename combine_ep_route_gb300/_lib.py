@@ -31,6 +31,8 @@ EP_STATIC_SCRATCH_BYTES = 4 << 20
 
 EP_BF16 = 1
 EP_F32 = 2
+EP_FP8 = 3
+EP_FP4X2 = 4
 
 EP_PATH_FUSED = 0
 EP_PATH_SENDBUF = 1

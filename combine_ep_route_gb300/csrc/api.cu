@@ -18,22 +18,37 @@ constexpr int kIdle = 0, kDispatched = 1;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bytes of one dispatched activation row: bf16 (2 per element), fp8 (1) or
+// packed fp4 (two elements per byte). 0 for an unknown type.
+long long x_row_bytes(const ep_config_t *c) {
+    switch (c->x_dtype) {
+        case EP_BF16: return 2LL * c->hidden;
+        case EP_FP8: return (long long)c->hidden;
+        case EP_FP4X2: return c->hidden % 2 ? 0 : c->hidden / 2;
+        default: return 0;
+    }
+}
+
 bool config_ok(const ep_config_t *c) {
     if (!c) return false;
     if (c->W < 1 || c->W > EP_MAX_W) return false;
     if (c->E < c->W || c->E > EP_MAX_E || c->E % c->W != 0) return false;
     if (c->top_k < 1 || c->top_k > EP_MAX_TOPK || c->top_k > c->E) return false;
+    // hidden: the bf16 rows of expert_out and out need 2*h % 16 == 0; the
+    // dispatched rows (bf16, fp8 or packed fp4) must be whole 16-byte vectors too
     if (c->max_tokens < 1 || c->hidden < 8 || (2LL * c->hidden) % 16 != 0) return false;
-    if (c->x_dtype != EP_BF16) return false;
+    const long long xb = x_row_bytes(c);
+    if (xb <= 0 || xb % 16 != 0) return false;
     if (c->n_extra < 0 || c->n_extra > EP_MAX_EXTRA) return false;
-    long long rb = 2LL * c->hidden;
+    long long rb = xb;
     for (int i = 0; i < c->n_extra; ++i) {
         if (c->extra_row_bytes[i] <= 0 || c->extra_row_bytes[i] % 16 != 0) return false;
         rb += c->extra_row_bytes[i];
     }
     if (c->flags & ~(EP_FLAG_ZERO_PAD | EP_FLAG_SENDBUF | EP_FLAG_WEIGHT_ON_INPUT)) return false;
-    // the page applies router weights on input for top_k == 1 only
-    if ((c->flags & EP_FLAG_WEIGHT_ON_INPUT) && c->top_k != 1) return false;
+    // the page applies router weights on input for top_k == 1 only (and scales bf16 rows)
+    if ((c->flags & EP_FLAG_WEIGHT_ON_INPUT) && (c->top_k != 1 || c->x_dtype != EP_BF16))
+        return false;
     // a row must fit twice into one mover CTA's stage memory
     if (2 * align_up((size_t)rb, 128) > ep::kMoveSmemBudget) return false;
     // flat expert row indices (E * Ecap) and flat pair indices stay within int32
@@ -53,7 +68,7 @@ void compute_layout(const ep_config_t *c, Layout *L) {
     L->tiles_per_rank = (Tm + ep::kRouteTile - 1) / ep::kRouteTile;
     L->num_tiles = W * L->tiles_per_rank;
     L->n_ctr = W + c->E;
-    uint32_t rb = 2u * (uint32_t)c->hidden;
+    uint32_t rb = (uint32_t)x_row_bytes(c);
     for (int i = 0; i < c->n_extra; ++i) rb += (uint32_t)c->extra_row_bytes[i];
     L->row_bytes = rb;
     size_t off = 0;
@@ -177,7 +192,7 @@ void fill_move_common(const ep_ctx *c, ep::MoveParams &m) {
     m.e_local = c->L.e_local;
     m.Ecap = c->L.Ecap;
     m.n_seg = 1 + cf.n_extra;
-    m.seg_bytes[0] = 2u * (uint32_t)cf.hidden;
+    m.seg_bytes[0] = (uint32_t)x_row_bytes(&cf);
     m.seg_off[0] = 0;
     for (int i = 0; i < cf.n_extra; ++i) {
         m.seg_bytes[1 + i] = (uint32_t)cf.extra_row_bytes[i];
@@ -205,7 +220,7 @@ void fill_move_common(const ep_ctx *c, ep::MoveParams &m) {
 // Chunks per row: the largest count whose chunk is at least the target size
 // and a multiple of 16 bytes that divides the activation row.
 int move_chunks(const ep_ctx *c) {
-    const uint32_t a1b = 2u * (uint32_t)c->cfg.hidden;
+    const uint32_t a1b = (uint32_t)x_row_bytes(&c->cfg);
     if (c->move_chunk_target == 0) return 1;
     int best = 1;
     for (int n = 2; n <= 64; ++n) {
@@ -218,7 +233,7 @@ int move_chunks(const ep_ctx *c) {
 
 void move_shape(const ep_ctx *c, int chunks, int &pipes, int &stages, uint32_t &stage_bytes,
                 size_t &smem) {
-    const uint32_t a1b = 2u * (uint32_t)c->cfg.hidden;
+    const uint32_t a1b = (uint32_t)x_row_bytes(&c->cfg);
     stage_bytes = (uint32_t)align_up(a1b / chunks + (c->L.row_bytes - a1b), 128);
     const int ctas = c->move_ctas_per_sm;
     size_t budget = ctas == 1 ? ep::kMoveSmemBudget : (size_t)(220 * 1024) / ctas - 2048;
@@ -534,7 +549,7 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         ep::ZeroPadParams zp;
         std::memset(&zp, 0, sizeof(zp));
         zp.n_seg = 1 + cf.n_extra;
-        zp.seg_bytes[0] = 2u * (uint32_t)cf.hidden;
+        zp.seg_bytes[0] = (uint32_t)x_row_bytes(&cf);
         zp.dst_seg[0] = static_cast<uint8_t *>(b_a1);
         for (int i = 0; i < cf.n_extra; ++i) {
             zp.seg_bytes[1 + i] = (uint32_t)cf.extra_row_bytes[i];
@@ -543,6 +558,13 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         zp.expert_num_tokens = expert_num_tokens;
         zp.E = cf.E;
         zp.Ecap = L.Ecap;
+        zp.send_cnt = ws_ptr<int32_t>(ctx, L.send_cnt);
+        zp.recv_eloc = ws_ptr<int32_t>(ctx, L.recv_eloc);
+        zp.recv_w = ws_ptr<float>(ctx, L.recv_w);
+        zp.recv_row = ws_ptr<int32_t>(ctx, L.recv_row);
+        zp.W = cf.W;
+        zp.Tm = cf.max_tokens;
+        zp.S = L.S;
         KernelTimer tm(ctx, EP_K_ZERO_PAD, st);
         if (ep::launch_zero_pad(zp, 32, st) != cudaSuccess) return EP_ERR_CUDA;
     }

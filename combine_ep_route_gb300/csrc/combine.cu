@@ -358,8 +358,29 @@ __global__ void __launch_bounds__(256) zero_pad_kernel(const ZeroPadParams p) {
     }
 }
 
+// Received slots at or past a source's count get the page's fill: local id -1,
+// weight 0, row -1 (its send_eloc / send_w start as full(-1) / zeros).
+__global__ void __launch_bounds__(256) sanitize_recv_kernel(const ZeroPadParams p) {
+    const size_t n = (size_t)p.W * p.W * p.Tm;
+    for (size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x; r < n;
+         r += (size_t)gridDim.x * blockDim.x) {
+        const int slot = (int)(r % p.Tm);
+        const size_t ds = r / p.Tm;
+        const int d = (int)(ds / p.W), s = (int)(ds % p.W);
+        if (slot < p.send_cnt[s * p.W + d]) continue;
+        for (int c = 0; c < p.S; ++c) {
+            p.recv_eloc[r * p.S + c] = -1;
+            p.recv_w[r * p.S + c] = 0.f;
+            p.recv_row[r * p.S + c] = -1;
+        }
+    }
+}
+
 cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st) {
     zero_pad_kernel<<<dim3(grid_x, p.E), 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    sanitize_recv_kernel<<<grid_x * 8, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

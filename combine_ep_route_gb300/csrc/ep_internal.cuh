@@ -164,6 +164,11 @@ struct ZeroPadParams {
     uint8_t *dst_seg[kMaxSeg];
     const int32_t *expert_num_tokens;   // [E]
     int E, Ecap;
+    // received-slot metadata past the counts gets the page's fill values
+    const int32_t *send_cnt;
+    int32_t *recv_eloc, *recv_row;
+    float *recv_w;
+    int W, Tm, S;
 };
 
 // --------------------------------------------------------------- device utils

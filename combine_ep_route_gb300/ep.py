@@ -30,6 +30,20 @@ class EpConfig:
     zero_pad: bool = False
     sendbuf: bool = False
     weight_on_input: bool = False   # apply_router_weight_on_input (top_k == 1)
+    x_dtype: str = "bf16"           # dispatched rows: "bf16", "fp8" or "fp4x2" (packed pairs)
+
+    @property
+    def x_row_bytes(self) -> int:
+        return {"bf16": 2 * self.hidden, "fp8": self.hidden, "fp4x2": self.hidden // 2}[self.x_dtype]
+
+    @property
+    def x_torch_dtype(self):
+        """Torch dtype of a1 / b_a1 rows (packed fp4 rows are uint8 bytes)."""
+        return {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn, "fp4x2": torch.uint8}[self.x_dtype]
+
+    @property
+    def x_row_elems(self) -> int:
+        return self.hidden if self.x_dtype != "fp4x2" else self.hidden // 2
 
     @property
     def e_local(self) -> int:
@@ -38,7 +52,7 @@ class EpConfig:
     def to_c(self) -> L.EpConfigC:
         c = L.EpConfigC()
         c.W, c.E, c.top_k, c.max_tokens, c.hidden = self.W, self.E, self.top_k, self.max_tokens, self.hidden
-        c.x_dtype = L.EP_BF16
+        c.x_dtype = {"bf16": L.EP_BF16, "fp8": L.EP_FP8, "fp4x2": L.EP_FP4X2}[self.x_dtype]
         c.n_extra = len(self.extra_row_bytes)
         for i, b in enumerate(self.extra_row_bytes):
             c.extra_row_bytes[i] = int(b)
@@ -105,7 +119,8 @@ class EpContext:
     # ------------------------------------------------------------ buffers
     def alloc_dispatch_outputs(self) -> DispatchOut:
         c = self.cfg
-        b = torch.empty((c.W, c.e_local, self.expert_cap, c.hidden), dtype=torch.bfloat16, device=self.device)
+        b = torch.empty((c.W, c.e_local, self.expert_cap, c.x_row_elems), dtype=c.x_torch_dtype,
+                        device=self.device)
         n = torch.empty((c.W, c.e_local), dtype=torch.int32, device=self.device)
         ex = [torch.empty((c.W, c.e_local, self.expert_cap, nb), dtype=torch.uint8, device=self.device)
               for nb in c.extra_row_bytes]
@@ -118,7 +133,7 @@ class EpContext:
                  stream: Optional[torch.cuda.Stream] = None) -> DispatchOut:
         """Route, deduplicate, slot and deliver all W ranks' tokens (``prepare``)."""
         c, dev = self.cfg, self.device
-        _need(a1, "a1", torch.bfloat16, (c.W, c.max_tokens, c.hidden), dev)
+        _need(a1, "a1", c.x_torch_dtype, (c.W, c.max_tokens, c.x_row_elems), dev)
         _need(topk_ids, "topk_ids", torch.int32, (c.W, c.max_tokens, c.top_k), dev)
         _need(topk_weights, "topk_weights", torch.float32, (c.W, c.max_tokens, c.top_k), dev)
         if num_tokens is not None:
@@ -130,7 +145,7 @@ class EpContext:
                 raise ValueError(f"extras[{i}]: want contiguous [W, Tm, {nb} bytes] on {dev}")
         if out is None:
             out = self.alloc_dispatch_outputs()
-        _need(out.b_a1, "b_a1", torch.bfloat16, (c.W, c.e_local, self.expert_cap, c.hidden), dev)
+        _need(out.b_a1, "b_a1", c.x_torch_dtype, (c.W, c.e_local, self.expert_cap, c.x_row_elems), dev)
         _need(out.expert_num_tokens, "expert_num_tokens", torch.int32, (c.W, c.e_local), dev)
         n_ex = len(c.extra_row_bytes)
         ein = (C.c_void_p * max(n_ex, 1))(*[x.data_ptr() for x in extras])

@@ -22,11 +22,11 @@
  *     NULL = the legacy default stream) with no host synchronisation, except in
  *     ep_status and ep_kernel_times, which synchronise.
  *   - Layouts are dense, row-major, with a leading rank dimension [W]:
- *       a1            [W][Tm][h]            bf16
+ *       a1            [W][Tm][h]            x_dtype (bf16; or fp8 / packed fp4 bytes)
  *       topk_ids      [W][Tm][K]            int32, negative = no expert
  *       topk_weights  [W][Tm][K]            float32
  *       num_tokens    [W]                   int32 (rank r holds tokens 0..num_tokens[r]-1)
- *       b_a1          [W][e_local][Ecap][h] bf16, the batched-experts layout
+ *       b_a1          [W][e_local][Ecap][h] x_dtype, the batched-experts layout
  *       expert_num_tokens [W][e_local]      int32
  *       extra_in[i]   [W][Tm][extra_row_bytes[i]]        opaque bytes
  *       extra_out[i]  [W][e_local][Ecap][extra_row_bytes[i]]
@@ -67,8 +67,10 @@ extern "C" {
 #define EP_ERR_CUDA -8        /* a CUDA runtime call or kernel launch failed */
 
 /* ------------------------------------------------------------------- dtypes */
-#define EP_BF16 1
-#define EP_F32 2
+#define EP_BF16 1  /* activation rows / outputs: 2 bytes per element */
+#define EP_F32 2   /* combine output: 4 bytes per element */
+#define EP_FP8 3   /* dispatched activation rows as 1-byte elements (e.g. fp8 e4m3); opaque here */
+#define EP_FP4X2 4 /* dispatched activation rows as packed 4-bit pairs (h/2 bytes); opaque here */
 
 /* ----------------------------------------------------------- dispatch paths */
 #define EP_PATH_FUSED 0   /* a1 -> b_a1 directly, each token row read once */
@@ -76,8 +78,10 @@ extern "C" {
 
 /* ---------------------------------------------------------------- flags */
 #define EP_FLAG_ZERO_PAD 1u /* dispatch also zeroes b_a1 / extra_out rows at or past
-                               expert_num_tokens (the page zero-fills them); otherwise
-                               those rows are left as they were */
+                               expert_num_tokens (the page zero-fills them) and resets the
+                               received-slot metadata of slots past the counts to the page's
+                               fill (local id -1, weight 0, row -1); otherwise those rows and
+                               slots are left as they were */
 #define EP_FLAG_SENDBUF 2u  /* size the workspace for EP_PATH_SENDBUF as well */
 #define EP_FLAG_WEIGHT_ON_INPUT 4u /* apply_router_weight_on_input of `prepare`: top_k must be
                                       1; dispatch delivers bf16(a1 * bf16(w)) and carries unit
@@ -88,8 +92,12 @@ typedef struct ep_config {
     int32_t E;          /* experts in total, a multiple of W, <= EP_MAX_E */
     int32_t top_k;      /* experts per token, 1..min(E, EP_MAX_TOPK) */
     int32_t max_tokens; /* token slots per rank (Tm), >= 1 */
-    int32_t hidden;     /* h, elements per a1 row; 2*h must be a multiple of 16 */
-    int32_t x_dtype;    /* EP_BF16 */
+    int32_t hidden;     /* h, elements per row; 2*h and the dispatched row bytes must be
+                           multiples of 16 */
+    int32_t x_dtype;    /* dispatched a1 / b_a1 element type: EP_BF16, EP_FP8 or EP_FP4X2.
+                           Quantised rows (the page's one-sided sizing: nvfp4 h/2 bytes plus
+                           fp8 block scales) travel as opaque bytes; scales go as extra
+                           payloads. expert_out and out of combine stay bf16 / f32. */
     int32_t n_extra;    /* extra payloads, 0..EP_MAX_EXTRA */
     int32_t extra_row_bytes[EP_MAX_EXTRA]; /* each a positive multiple of 16 */
     uint32_t flags;     /* EP_FLAG_* */

@@ -23,9 +23,10 @@ def lib():
     return L.lib()
 
 
-def cfg(W=8, E=64, K=8, T=128, h=2048, extras=(), flags=0, n_extra=None):
+def cfg(W=8, E=64, K=8, T=128, h=2048, extras=(), flags=0, n_extra=None, x_dtype=None):
     c = L.EpConfigC()
-    c.W, c.E, c.top_k, c.max_tokens, c.hidden, c.x_dtype = W, E, K, T, h, L.EP_BF16
+    c.W, c.E, c.top_k, c.max_tokens, c.hidden = W, E, K, T, h
+    c.x_dtype = L.EP_BF16 if x_dtype is None else x_dtype
     c.n_extra = len(extras) if n_extra is None else n_extra
     for i, b in enumerate(extras):
         c.extra_row_bytes[i] = b
@@ -65,6 +66,8 @@ def test_capacities_match_oracle(lib, W, E, K, T):
     dict(W=0), dict(W=65, E=1040), dict(E=60), dict(E=2048), dict(K=0), dict(K=17), dict(T=0),
     dict(h=4), dict(h=12), dict(extras=(20,)), dict(extras=(16,) * 4, n_extra=5), dict(n_extra=-1), dict(flags=8),
     dict(h=60000), dict(W=64, E=1024, T=40000), dict(K=2, flags=4),
+    dict(x_dtype=9), dict(x_dtype=L.EP_FP8, h=24), dict(x_dtype=L.EP_FP4X2, h=40),
+    dict(K=1, flags=4, x_dtype=L.EP_FP8),
 ])
 def test_invalid_configs_rejected(lib, bad):
     n = C.c_size_t()
@@ -74,6 +77,15 @@ def test_invalid_configs_rejected(lib, bad):
     assert lib.ep_capacities(C.byref(c), C.byref(a), C.byref(a), C.byref(a)) == L.EP_ERR_INVALID_ARG
     h = C.c_void_p()
     assert lib.ep_ctx_create(C.byref(c), C.c_void_p(FAKE_WS), 1 << 40, C.byref(h)) == L.EP_ERR_INVALID_ARG
+
+
+def test_quantised_row_types_size_the_send_rows(lib):
+    for xd, rb in [(L.EP_BF16, 4096), (L.EP_FP8, 2048), (L.EP_FP4X2, 1024)]:
+        h, _ = _ctx(lib, cfg(x_dtype=xd, extras=(128,), flags=L.EP_FLAG_SENDBUF))
+        m = L.EpMetadataC()
+        assert lib.ep_get_metadata(h, C.byref(m)) == 0
+        assert m.row_bytes == rb + 128
+        lib.ep_ctx_destroy(h)
 
 
 def test_workspace_sizing(lib):

@@ -139,6 +139,11 @@ def test_zero_pad_flag(dev):
     for e in range(s.E):
         n = int(m.expert_num_tokens.reshape(-1)[e])
         assert (b[e, n:] == 0).all()
+    # received-slot metadata past the counts carries the page's fill values
+    md = ctx.metadata()
+    assert np.array_equal(md["recv_eloc"].cpu().numpy(), m.recv_eloc)
+    assert np.array_equal(md["recv_w"].cpu().numpy(), m.recv_w)
+    assert np.array_equal(md["recv_row"].cpu().numpy(), H.expected_recv_row(m))
 
 
 def test_device_errors_are_reported_and_pairs_dropped(dev):
@@ -308,3 +313,45 @@ def test_graph_replay_on_new_inputs(dev):
         H.check_rows(out, m, x, a1, [])
         exp = ref.combine(m, x.topk_weights, ref.dispatch_rows(m, x.a1))
         assert np.array_equal(H.bits_host(y).reshape(-1, s.h), exp)
+
+
+@pytest.mark.parametrize("x_dtype,extra_cols", [("fp8", 56), ("fp4x2", 112)])
+@pytest.mark.parametrize("path", ["fused", "sendbuf"])
+def test_quantised_payload_rows(dev, x_dtype, extra_cols, path):
+    """Quantised activations as the page's one-sided sizing assumes (fp8 rows of h
+    bytes with fp32 block scales, or packed fp4 rows of h/2 bytes with 4-byte scale
+    words) travel as opaque bytes; rows and scales land byte-exact, and combine
+    still reduces bf16 expert outputs."""
+    base = wl.make(wl.spec(3, T=64))
+    s = base.spec
+    rng = np.random.default_rng(17)
+    row_bytes = s.h if x_dtype == "fp8" else s.h // 2
+    a1_bytes = rng.integers(0, 256, size=(s.W, s.T, row_bytes), dtype=np.uint8)
+    scales = rng.integers(0, 256, size=(s.W, s.T, extra_cols * 4), dtype=np.uint8)
+    from combine_ep_route_gb300 import EpConfig, EpContext
+    cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=(extra_cols * 4,), sendbuf=path == "sendbuf",
+                   x_dtype=x_dtype)
+    ctx = EpContext(cfg, dev)
+    a1 = torch.from_numpy(a1_bytes).to(dev).view(cfg.x_torch_dtype)
+    ids = torch.from_numpy(base.topk_ids).to(dev)
+    w = torch.from_numpy(base.topk_weights).to(dev)
+    ex = [torch.from_numpy(scales).to(dev)]
+    out = ctx.dispatch(a1, ids, w, extras=ex, path=path)
+    ctx.check()
+    m = H.oracle_meta(base)
+    rows = ref.dispatch_rows(m, np.concatenate([a1_bytes, scales], axis=2))
+    flat, _ = H.valid_rows(m)
+    fi = torch.from_numpy(flat).to(dev)
+    got = out.b_a1.view(torch.uint8).view(-1, row_bytes).index_select(0, fi).cpu().numpy()
+    assert np.array_equal(got, rows[:, :row_bytes])
+    got_sc = out.extra_out[0].view(-1, extra_cols * 4).index_select(0, fi).cpu().numpy()
+    assert np.array_equal(got_sc, rows[:, row_bytes:])
+    # combine on bf16 expert outputs of the delivered rows
+    expert_out = torch.zeros((s.W, s.E // s.W, ctx.expert_cap, s.h), dtype=torch.bfloat16, device=dev)
+    holder = type("O", (), {})()
+    holder.b_a1 = expert_out
+    packed = H.fill_pool_rows(holder, m, s.h, 6)
+    y = ctx.combine(expert_out)
+    ctx.check()
+    exp = ref.combine(m, base.topk_weights, packed)
+    assert np.array_equal(H.bits_host(y).reshape(-1, s.h), exp)
