@@ -50,12 +50,13 @@ EP_OPT_FAULT_SKIP_PUBLISH = 6
 EP_OPT_COMBINE_CTAS_PER_SM = 7
 EP_OPT_MOVE_CHUNK_BYTES = 8
 EP_OPT_MOVE_MAX_STAGES = 9
+EP_OPT_FUSED_DISPATCH = 10
 
 (EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD,
- EP_K_COMBINE_TWO_STAGE) = range(8)
-EP_K_COUNT = 8
+ EP_K_COMBINE_TWO_STAGE, EP_K_DISPATCH_FUSED) = range(9)
+EP_K_COUNT = 9
 KERNEL_NAMES = ("route", "move_fused", "pack", "exchange", "deliver", "combine", "zero_pad",
-                "combine_two_stage")
+                "combine_two_stage", "dispatch_fused")
 
 
 class EpConfigC(C.Structure):

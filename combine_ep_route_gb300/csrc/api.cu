@@ -117,6 +117,7 @@ struct ep_ctx {
     int move_pipes;
     int fault_skip;
     int combine_ctas_per_sm;
+    int fused_dispatch;      // routing and row movement in one persistent launch
     int move_chunk_target;   // bytes; 0 = whole rows
     int move_max_stages;
     // counters and event timing
@@ -246,12 +247,12 @@ void move_shape(const ep_ctx *c, int chunks, int &pipes, int &stages, uint32_t &
     if (stages < 2) stages = 2;
     const int W = c->cfg.W;
     smem = (size_t)pipes * stages * stage_bytes + (size_t)pipes * stages * 8 +
-           (size_t)pipes * stages * (ep::kMaxDst + 2) * 4 + (size_t)(W * W + 1) * 4;
+           (size_t)pipes * stages * (ep::kMaxDst + 3) * 4 + (size_t)(W * W + 1) * 4;
 }
 
-int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *const *extra_in,
-                     void *b_a1, void *const *extra_out, bool pdl, cudaStream_t st) {
-    ep::MoveParams m;
+// Mover parameters and launch shape for one mode.
+void build_move(ep_ctx *c, int mode, const void *a1, const void *const *extra_in, void *b_a1,
+                void *const *extra_out, ep::MoveParams &m, int &grid, int &block, size_t &smem_out) {
     fill_move_common(c, m);
     m.src_seg[0] = static_cast<const uint8_t *>(a1);
     m.dst_seg[0] = static_cast<uint8_t *>(b_a1);
@@ -272,9 +273,19 @@ int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *
     m.stage_bytes = stage_bytes;
     m.chunks = chunks;
     m.chunk_bytes = m.seg_bytes[0] / (uint32_t)m.chunks;
-    const int grid = c->num_sms * c->move_ctas_per_sm;
+    grid = c->num_sms * c->move_ctas_per_sm;
+    block = pipes * 32;
+    smem_out = smem;
+}
+
+int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *const *extra_in,
+                     void *b_a1, void *const *extra_out, bool pdl, cudaStream_t st) {
+    ep::MoveParams m;
+    int grid, block;
+    size_t smem;
+    build_move(c, mode, a1, extra_in, b_a1, extra_out, m, grid, block, smem);
     KernelTimer tm(c, kind, st);
-    return ep::launch_move(mode, m, grid, pipes * 32, smem, pdl && !c->timing, st) == cudaSuccess
+    return ep::launch_move(mode, m, grid, block, smem, pdl && !c->timing, st) == cudaSuccess
                ? EP_OK
                : EP_ERR_CUDA;
 }
@@ -341,6 +352,7 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->move_pipes = 8;
     c->fault_skip = -1;
     c->combine_ctas_per_sm = 0;   // 0 = as many as fit (occupancy)
+    c->fused_dispatch = 1;
     c->move_chunk_target = 2048;
     c->move_max_stages = 4;
     for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
@@ -404,6 +416,10 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
         case EP_OPT_MOVE_MAX_STAGES:
             if (value < 2 || value > 32) return EP_ERR_INVALID_ARG;
             ctx->move_max_stages = (int)value;
+            return EP_OK;
+        case EP_OPT_FUSED_DISPATCH:
+            if (value != 0 && value != 1) return EP_ERR_INVALID_ARG;
+            ctx->fused_dispatch = (int)value;
             return EP_OK;
         default: return EP_ERR_INVALID_ARG;
     }
@@ -484,12 +500,39 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     rp.vec_ids = aligned(topk_ids, 16) && aligned(topk_weights, 16);
     rp.vec_recv = L.S % 4 == 0;   // workspace regions are 256-byte aligned
     rp.unit_weights = (cf.flags & EP_FLAG_WEIGHT_ON_INPUT) ? 1 : 0;
-    {
+    const bool pdl = ctx->pdl != 0;
+    bool one_launch = ctx->fused_dispatch && path == EP_PATH_FUSED &&
+                      !(cf.flags & EP_FLAG_WEIGHT_ON_INPUT);
+    ep::MoveParams fm;
+    int fgrid = 0, fblock = 0;
+    size_t fsmem = 0;
+    if (one_launch) {
+        // routing and row movement in one persistent launch needs one CTA per SM
+        // with eight pipelines (the routing step's 256 threads); rows too large
+        // for eight pipelines' stages take the two-launch path
+        const int saved_pipes = ctx->move_pipes, saved_ctas = ctx->move_ctas_per_sm;
+        ctx->move_pipes = ep::kRouteThreads / 32;
+        ctx->move_ctas_per_sm = 1;
+        build_move(ctx, ep::MOVE_FUSED, a1, extra_in, b_a1, extra_out, fm, fgrid, fblock, fsmem);
+        ctx->move_pipes = saved_pipes;
+        ctx->move_ctas_per_sm = saved_ctas;
+        one_launch = fblock == ep::kRouteThreads;
+    }
+    if (one_launch) {
+        fm.wait_tiles = 1;
+        fm.dynamic_units = 1;
+        fm.tile_flag = rp.tile_flag;
+        fm.tiles_per_rank = L.tiles_per_rank;
+        fm.div_tm = ep::make_fastdiv((uint32_t)cf.max_tokens);
+        KernelTimer tm(ctx, EP_K_DISPATCH_FUSED, st);
+        if (ep::launch_dispatch_fused(rp, fm, ctx->num_sms, fsmem, st) != cudaSuccess) return EP_ERR_CUDA;
+    } else {
         KernelTimer tm(ctx, EP_K_ROUTE, st);
         if (ep::launch_route(rp, st) != cudaSuccess) return EP_ERR_CUDA;
     }
-    const bool pdl = ctx->pdl != 0;
-    if (cf.flags & EP_FLAG_WEIGHT_ON_INPUT) {
+    if (one_launch) {
+        // rows already moved
+    } else if (cf.flags & EP_FLAG_WEIGHT_ON_INPUT) {
         // rows are scaled while they move: one register-path kernel to the b_a1
         // row (fused) or to the send row (send-buffer path, then the mover)
         ep::ScaleMoveParams sp;

@@ -28,7 +28,8 @@ struct DevHeader {
     uint32_t ticket;      // routing tiles started in this launch (reset by the last tile)
     uint32_t done;        // routing tiles finished in this launch
     uint32_t epoch;       // look-back epoch of the running launch; the last tile advances it
-    uint32_t pad[59];
+    uint32_t move_next;   // next row-mover unit handed out (fused dispatch; reset at the end)
+    uint32_t pad[58];
 };
 static_assert(sizeof(DevHeader) == 256, "header is one aligned block");
 
@@ -59,6 +60,27 @@ struct RouteParams {
     int32_t unit_weights;        // weights applied on input: carry 1.0 instead of w
 };
 
+// Division by a run-time invariant d via multiply and shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// for d >= 1 and 0 <= n < 2^31, n / d == (umulhi(n, m) + n) >> l with
+// l = ceil(log2 d) and m = floor(2^32 * (2^l - d) / d) + 1.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = (uint32_t)((((1ull << f.l) - d) << 32) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv &f) {
+    return (__umulhi(n, f.m) + n) >> f.l;
+}
+
 enum MoveMode { MOVE_FUSED = 0, MOVE_PACK = 1, MOVE_EXCHANGE = 2, MOVE_DELIVER = 3 };
 
 struct MoveParams {
@@ -80,28 +102,13 @@ struct MoveParams {
     uint32_t stage_bytes;
     DevHeader *hdr;
     uint64_t wait_limit_ns;
+    // routing in the same launch: wait for a token's tile before reading its rows
+    int wait_tiles;
+    int dynamic_units;                  // warps grab units from hdr->move_next
+    const uint32_t *tile_flag;
+    int tiles_per_rank;
+    FastDiv div_tm;
 };
-
-// Division by a run-time invariant d via multiply and shift (Granlund and
-// Montgomery, "Division by invariant integers using multiplication", 1994):
-// for d >= 1 and 0 <= n < 2^31, n / d == (umulhi(n, m) + n) >> l with
-// l = ceil(log2 d) and m = floor(2^32 * (2^l - d) / d) + 1.
-struct FastDiv {
-    uint32_t d, m, l;
-};
-
-inline FastDiv make_fastdiv(uint32_t d) {
-    FastDiv f;
-    f.d = d;
-    f.l = 0;
-    while ((1ull << f.l) < d) ++f.l;
-    f.m = (uint32_t)((((1ull << f.l) - d) << 32) / d + 1);
-    return f;
-}
-
-__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv &f) {
-    return (__umulhi(n, f.m) + n) >> f.l;
-}
 
 struct CombineParams {
     const uint8_t *expert_out;   // [E*Ecap][h] bf16
@@ -295,6 +302,9 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 size_t route_smem_bytes(int n_ctr, int top_k);
 cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size_t smem, bool pdl,
                         cudaStream_t st);
+// Routing and the fused row movement in one persistent launch (grid = resident CTAs).
+cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, int grid,
+                                  size_t move_smem, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st);
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);

@@ -20,11 +20,30 @@
 // with k destinations is read from HBM once. A unit is one chunk of a row's
 // activation part (the extra payloads travel with chunk 0): many equal units
 // per pipeline keep the tail of the persistent grid short.
-#include "ep_internal.cuh"
+#include "route_tile.cuh"
 
 namespace ep {
 
 namespace {
+
+// Wait (bounded) until a routing tile of this launch has published its
+// outputs. False after the limit (EP_ERR_TIMEOUT raised).
+__device__ __forceinline__ bool wait_tile_done(const uint32_t *f, uint32_t epoch, uint64_t limit_ns,
+                                               DevHeader *hdr) {
+    const uint32_t want = (epoch << 2) | kFlagDone;
+    if (ld_acquire_u32(f) == want) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t back = 64;
+    for (;;) {
+        __nanosleep(back);
+        if (back < 1024) back <<= 1;
+        if (ld_acquire_u32(f) == want) return true;
+        if (global_ns() - t0 > limit_ns) {
+            raise_error(hdr, EP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
 
 // Largest b in [0, nb) with pre[b] <= u, for pre[0] = 0 <= u < pre[nb].
 __device__ __forceinline__ int find_block(const int32_t *pre, int nb, int u) {
@@ -41,10 +60,30 @@ __device__ __forceinline__ int find_block(const int32_t *pre, int nb, int u) {
 // index (-1 for none) of unit u.
 template <int MODE>
 __device__ __forceinline__ void unit_meta(const MoveParams &p, const int32_t *pre, int u, int lane,
-                                          int &src, int &dst) {
+                                          uint32_t epoch, int &src, int &dst) {
     dst = -1;
     if (MODE == MOVE_FUSED || MODE == MOVE_PACK) {
         src = u;
+        if (p.wait_tiles) {
+            // routing runs in this launch: wait (bounded) until the token's tile
+            // has published its outputs, then read them past the L1
+            const uint32_t s = fastdiv((uint32_t)u, p.div_tm);
+            const int t = u - (int)s * p.Tm;
+            const uint32_t *flag = p.tile_flag + (int)s * p.tiles_per_rank + t / kRouteTile;
+            bool ready = true;
+            if (lane == 0) ready = wait_tile_done(flag, epoch, p.wait_limit_ns, p.hdr);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (ready && lane < p.K) {
+                (void)ld_acquire_u32(flag);   // each reading lane acquires the tile's release
+                dst = __ldcg((MODE == MOVE_FUSED ? p.pair_row : p.pair_send) + (size_t)u * p.K + lane);
+                const int lim = MODE == MOVE_FUSED ? p.n_rows : p.n_slots;
+                if (dst >= lim) {
+                    raise_error(p.hdr, EP_ERR_STATE);
+                    dst = -1;
+                }
+            }
+            return;
+        }
         if (lane < p.K) {
             dst = (MODE == MOVE_FUSED ? p.pair_row : p.pair_send)[(size_t)u * p.K + lane];
             const int lim = MODE == MOVE_FUSED ? p.n_rows : p.n_slots;
@@ -80,10 +119,10 @@ __device__ __forceinline__ void unit_meta(const MoveParams &p, const int32_t *pr
 
 }  // namespace
 
+// The mover's pipelines over one CTA's share of the units (see the top of the file).
 template <int MODE>
-__global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kStash = kMaxDst + 2;   // per stage: src, count, destinations
+__device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, uint32_t epoch) {
+    constexpr int kStash = kMaxDst + 3;   // per stage: src, count, destinations, chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int P = blockDim.x >> 5;
     const int NS = p.stages;
@@ -150,12 +189,42 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
     const uint32_t tail = p.row_bytes - a1b;   // extra payload bytes, moved with chunk 0
     const int n_work = n_units * C;
     const int first = blockIdx.x * P + warp, stride = gridDim.x * P;
-    const int my_n = n_work > first ? (n_work - first + stride - 1) / stride : 0;
 
+    // The warp's i-th unit: a fixed stride (static), or -- dynamic -- its first
+    // kStaticUnits units by stride and the rest in batches of kUnitBatch grabbed
+    // from a launch-wide counter, so a warp that starts late (after routing a
+    // tile in the same launch) takes fewer units, while small problems never
+    // touch the counter. Called with i growing by at most one per new value.
+    constexpr int kStaticUnits = 2, kUnitBatch = 4;
+    const bool dyn = p.dynamic_units != 0;
+    int seq_base = 0, seq_len = 0, seq_i0 = kStaticUnits;
+    auto unit_at = [&](int i) -> int {
+        if (!dyn || i < kStaticUnits) {
+            const int u = first + i * stride;
+            return u < n_work ? u : -1;
+        }
+        while (i >= seq_i0 + seq_len) {
+            if (seq_len < 0) return -1;   // the counter ran out
+            int b = 0;
+            if (lane == 0) b = (int)atomicAdd(&p.hdr->move_next, (uint32_t)kUnitBatch);
+            b = __shfl_sync(0xffffffffu, b, 0) + kStaticUnits * stride;
+            seq_i0 += seq_len;
+            if (b >= n_work) {
+                seq_len = -1;
+                return -1;
+            }
+            seq_base = b;
+            seq_len = min(kUnitBatch, n_work - b);
+        }
+        return seq_base + (i - seq_i0);
+    };
+
+    int nxt_u = unit_at(0);
     int nxt_src = -1, nxt_dst = -1;   // metadata of the next unit to load
-    if (my_n > 0) unit_meta<MODE>(p, pre, first / C, lane, nxt_src, nxt_dst);
+    if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
 
-    // Load unit i (the next one in order) into stage i % NS.
+    // Load the warp's unit i (the next one in order) into stage i % NS and
+    // prefetch the metadata of unit i + 1.
     auto issue = [&](int i) {
         const int st = i % NS;
         int32_t *sh = stash + st * kStash;
@@ -163,8 +232,10 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
         const uint32_t m = __ballot_sync(0xffffffffu, has);
         if (has) sh[2 + __popc(m & lanemask_lt())] = nxt_dst;
         const int src = nxt_src;
-        const int c = (first + i * stride) % C;
-        if (i + 1 < my_n) unit_meta<MODE>(p, pre, (first + (i + 1) * stride) / C, lane, nxt_src, nxt_dst);
+        const int c = nxt_u % C;
+        if (lane == 0) sh[kMaxDst + 2] = c;
+        nxt_u = unit_at(i + 1);
+        if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
         if (lane == 0) {
             sh[0] = m ? src : -1;
             sh[1] = __popc(m);
@@ -190,18 +261,18 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
         __syncwarp();
     };
 
-    const int pro = my_n < NS ? my_n : NS;
-    for (int i = 0; i < pro; ++i) issue(i);
+    int issued = 0;
+    while (issued < NS && nxt_u >= 0) issue(issued++);
     int consumed = 0;
     bool ok = true;
-    for (int i = 0; i < my_n; ++i) {
+    for (int i = 0; i < issued; ++i) {
         const int st = i % NS;
         if (lane == 0) {
             ok = mbar_wait_bounded(&bars[st], (uint32_t)(i / NS) & 1u, p.wait_limit_ns, p.hdr);
             const int32_t *sh = stash + st * kStash;
             if (ok && sh[0] >= 0) {
                 const uint8_t *stg = stages + (size_t)st * p.stage_bytes;
-                const int c = (first + i * stride) % C;
+                const int c = sh[kMaxDst + 2];
                 const int n = sh[1];
                 for (int q = 0; q < n; ++q) {
                     const size_t drow = (size_t)sh[2 + q];
@@ -223,24 +294,95 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         consumed = i + 1;
-        const int nx = i - 1 + NS;   // refill the stage unit i-1 used
-        if (i >= 1 && nx < my_n) {
+        // refill the stage unit i-1 used with the next unit, if there is one
+        if (i >= 1 && i - 1 + NS == issued && nxt_u >= 0) {
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
-            issue(nx);
+            issue(issued++);
         }
     }
     if (lane == 0) {
         if (!ok) {
             // drain the loads already issued before leaving (bounded)
-            // units issued so far: the prologue's, plus one refill per later iteration
-            int issued = consumed == 0 ? pro : consumed - 1 + NS;
-            if (issued > my_n) issued = my_n;
             for (int i = consumed + 1; i < issued; ++i)
                 if (!mbar_wait_bounded(&bars[i % NS], (uint32_t)(i / NS) & 1u, p.wait_limit_ns, p.hdr))
                     break;
         }
         bulk_wait_all();
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    move_body<MODE>(p, smem, 0u);
+}
+
+// Routing and the fused row movement in one persistent launch. Every CTA first
+// takes routing tiles by ticket until none is left, then moves rows; a unit
+// waits only for its own token's tile, so movement starts while later tiles
+// are still being routed. No deadlock: a unit waits only on a tile some
+// running CTA already owns (all tickets are taken before any CTA moves rows),
+// and tiles wait only on tiles with smaller tickets. The last CTA to finish
+// rearms the ticket and advances the look-back epoch, as the routing kernel does.
+template <int KT>
+__global__ void __launch_bounds__(256) dispatch_fused_kernel(const RouteParams rp, const MoveParams mp) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_q;
+    __shared__ uint32_t s_epoch;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_epoch = ld_acquire_u32(&rp.hdr->epoch) & 0x3FFFFFFFu;
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
+    for (;;) {
+        if (tid == 0) s_q = (int)atomicAdd(&rp.hdr->ticket, 1u);
+        __syncthreads();
+        const int q = s_q;
+        if (q >= rp.num_tiles) break;   // uniform across the CTA
+        route_tile<KT>(rp, q, epoch, reinterpret_cast<uint32_t *>(smem));
+    }
+    // shared memory now changes hands from the routing step (generic writes) to
+    // the mover's bulk copies (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    move_body<MOVE_FUSED>(mp, smem, epoch);   // mp.wait_tiles is set by the launcher
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&rp.hdr->done, 1u) == gridDim.x - 1) {
+            atomicExch(&rp.hdr->ticket, 0u);
+            atomicExch(&rp.hdr->move_next, 0u);
+            atomicExch(&rp.hdr->done, 0u);
+            atomicExch(&rp.hdr->epoch, (epoch + 1u) & 0x3FFFFFFFu);
+        }
+    }
+}
+
+template <int KT>
+static cudaError_t launch_dispatch_fused_kt(const RouteParams &rp, const MoveParams &mp, int grid,
+                                            size_t smem, cudaStream_t st) {
+    static size_t smem_set = 0;
+    if (smem > 48 * 1024 && smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_fused_kernel<KT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    dispatch_fused_kernel<KT><<<grid, kRouteThreads, smem, st>>>(rp, mp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, int grid,
+                                  size_t move_smem, cudaStream_t st) {
+    size_t smem = route_smem_bytes(rp.n_ctr, rp.K);
+    if (move_smem > smem) smem = move_smem;
+    switch (route_kt(rp.K)) {
+        case 1: return launch_dispatch_fused_kt<1>(rp, mp, grid, smem, st);
+        case 2: return launch_dispatch_fused_kt<2>(rp, mp, grid, smem, st);
+        case 4: return launch_dispatch_fused_kt<4>(rp, mp, grid, smem, st);
+        case 8: return launch_dispatch_fused_kt<8>(rp, mp, grid, smem, st);
+        case 16: return launch_dispatch_fused_kt<16>(rp, mp, grid, smem, st);
+        default: return cudaErrorInvalidValue;
     }
 }
 

@@ -265,6 +265,8 @@ const char *ep_error_string(int code);
 #define EP_OPT_MOVE_CHUNK_BYTES 8 /* row-mover unit: rows split into chunks of at least this
                                      many bytes (multiple of 16; 0 = whole rows; default 2048) */
 #define EP_OPT_MOVE_MAX_STAGES 9  /* row-mover stages per pipeline, at most (2..32, default 4) */
+#define EP_OPT_FUSED_DISPATCH 10  /* 1 (default): the fused path routes and moves rows in one
+                                     persistent launch, movement starting as tiles finish */
 
 /* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
 int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
@@ -278,7 +280,8 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
 #define EP_K_COMBINE 5
 #define EP_K_ZERO_PAD 6
 #define EP_K_COMBINE_TWO_STAGE 7
-#define EP_K_COUNT 8
+#define EP_K_DISPATCH_FUSED 8   /* routing + fused row movement in one launch */
+#define EP_K_COUNT 9
 
 typedef struct ep_kernel_times {
     int64_t launches[EP_K_COUNT]; /* kernels launched, per kind, since the last read */

@@ -211,6 +211,8 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     {L.EP_OPT_MOVE_CHUNK_BYTES: 2048, L.EP_OPT_MOVE_MAX_STAGES: 16},
     {L.EP_OPT_MOVE_CHUNK_BYTES: 1024, L.EP_OPT_MOVE_MAX_STAGES: 2, L.EP_OPT_MOVE_PIPES: 2},
     {L.EP_OPT_MOVE_CHUNK_BYTES: 0},
+    {L.EP_OPT_FUSED_DISPATCH: 0},
+    {L.EP_OPT_FUSED_DISPATCH: 0, L.EP_OPT_PDL: 1},
 ])
 @pytest.mark.parametrize("path", ["fused", "sendbuf"])
 def test_launch_options_do_not_change_results(dev, opts, path):
