@@ -318,6 +318,79 @@ void oracle_combine(int W, int E, int K, int Tm, int h, const int32_t *num_token
 }
 
 /*
+ * The all-gather / reduce-scatter route of vLLM's AgRsAll2AllManager (page
+ * device_communicators/all2all: `dispatch` gathers hidden states, top-k weights
+ * and ids of all ranks with all_gatherv; `combine` reduce-scatters), with the
+ * experts in between being the identity and each rank applying only its own
+ * experts, as the fused-MoE layer does with an expert map:
+ *   on rank d, for every gathered token g: y_d[g] = bf16( fp32 fold over the
+ *   token's kept pairs k whose expert lives on d, in top-k order, of w_k * x_g )
+ *   (zero if none);
+ *   reduce-scatter: out[g] = sum over d = 0..W-1 of y_d[g], in the output type
+ *   (bf16: every sum rounded; f32: fp32 sums).
+ * Pairs are kept by the same rule as oracle_route (negative ids dropped, ids
+ * >= E and repeats flagged and dropped). Tokens at or past num_tokens give 0.
+ */
+void oracle_agrs(int W, int E, int K, int Tm, int h, const int32_t *num_tokens,
+                 const int32_t *ids, const float *weights, const uint16_t *a1, int out_f32,
+                 void *out, uint32_t *err) {
+    int e_local = E / W;
+    float *yd = (float *)malloc(sizeof(float) * (size_t)h);
+    float *acc = (float *)malloc(sizeof(float) * (size_t)h);
+    int32_t *kept = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
+    for (int s = 0; s < W; ++s) {
+        int T = num_tokens ? num_tokens[s] : Tm;
+        if (T < 0 || T > Tm) {
+            *err |= OR_ERR_CAPACITY;
+            T = T < 0 ? 0 : Tm;
+        }
+        for (int t = 0; t < Tm; ++t) {
+            size_t g = (size_t)s * Tm + t;
+            for (int i = 0; i < h; ++i) acc[i] = 0.0f;
+            if (t < T) {
+                const int32_t *row = ids + g * K;
+                for (int k = 0; k < K; ++k) {
+                    int e = row[k];
+                    kept[k] = 0;
+                    if (e < 0) continue;
+                    if (e >= E) { *err |= OR_ERR_EXPERT_ID; continue; }
+                    int dup = 0;
+                    for (int k2 = 0; k2 < k; ++k2)
+                        if (kept[k2] && row[k2] == e) dup = 1;
+                    if (dup) { *err |= OR_ERR_DUPLICATE; continue; }
+                    kept[k] = 1;
+                }
+                for (int d = 0; d < W; ++d) {      /* every rank's expert output */
+                    for (int i = 0; i < h; ++i) yd[i] = 0.0f;
+                    for (int k = 0; k < K; ++k) {
+                        if (!kept[k] || row[k] / e_local != d) continue;
+                        float w = weights[g * K + k];
+                        for (int i = 0; i < h; ++i) {
+                            float p = w * bf16_to_f32(a1[g * h + i]);
+                            yd[i] = yd[i] + p;
+                        }
+                    }
+                    for (int i = 0; i < h; ++i) {    /* the reduce-scatter sum */
+                        float y = bf16_to_f32(f32_to_bf16(yd[i]));
+                        if (out_f32) acc[i] = acc[i] + y;
+                        else acc[i] = bf16_to_f32(f32_to_bf16(acc[i] + y));
+                    }
+                }
+            }
+            if (out_f32) {
+                memcpy((float *)out + g * h, acc, sizeof(float) * (size_t)h);
+            } else {
+                uint16_t *o = (uint16_t *)out + g * h;
+                for (int i = 0; i < h; ++i) o[i] = f32_to_bf16(acc[i]);
+            }
+        }
+    }
+    free(yd);
+    free(acc);
+    free(kept);
+}
+
+/*
  * `prepare` with apply_router_weight_on_input (the page allows it for top_k == 1
  * only): a1 is multiplied by the router weight converted to the activation
  * type, a1 = a1 * topk_weights.to(a1.dtype), so each element becomes

@@ -43,10 +43,11 @@ def lib():
         _lib.oracle_combine.argtypes = [i, i, i, i, i, P, P, P, P, P, i, P, P, C.c_int64]
         _lib.oracle_combine_pagemode.argtypes = [i, i, i, i, i, P, P, P, P, P, P, P, i, P]
         _lib.oracle_scale_input.argtypes = [C.c_int64, i, P, P, P]
+        _lib.oracle_agrs.argtypes = [i, i, i, i, i, P, P, P, P, i, P, P]
         for f in ("oracle_capacities", "oracle_route", "oracle_exchange_meta",
                   "oracle_deliver_meta", "oracle_pair_rows", "oracle_pack", "oracle_exchange",
                   "oracle_deliver", "oracle_combine", "oracle_combine_pagemode",
-                  "oracle_scale_input"):
+                  "oracle_scale_input", "oracle_agrs"):
             getattr(_lib, f).restype = None
     return _lib
 
@@ -233,3 +234,21 @@ def scale_input(a1: np.ndarray, topk_weights: np.ndarray) -> np.ndarray:
     out = np.empty_like(x)
     lib().oracle_scale_input(n, h, _p(x), _p(w), _p(out))
     return out
+
+
+def agrs(W: int, E: int, K: int, Tm: int, a1: np.ndarray, topk_ids: np.ndarray,
+         topk_weights: np.ndarray, num_tokens: Optional[np.ndarray] = None,
+         out_f32: bool = False):
+    """The all-gather / reduce-scatter route with identity experts (see
+    ``oracle_agrs``). Returns (out [W*Tm, h], error bits)."""
+    x = np.ascontiguousarray(a1).view(np.uint16).reshape(W * Tm, -1)
+    h = x.shape[1]
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32).reshape(W, Tm, K)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32).reshape(W, Tm, K)
+    nt = (np.full(W, Tm, dtype=np.int32) if num_tokens is None
+          else np.ascontiguousarray(num_tokens, dtype=np.int32).reshape(W))
+    out = np.zeros((W * Tm, h), np.float32 if out_f32 else np.uint16)
+    err = C.c_uint32(0)
+    lib().oracle_agrs(W, E, K, Tm, h, _p(nt), _p(ids), _p(w), _p(x), int(out_f32), _p(out),
+                      C.byref(err))
+    return out, int(err.value)

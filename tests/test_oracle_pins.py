@@ -406,3 +406,46 @@ def test_weight_on_input_scaling_closed_forms():
     exact = x.astype(np.float64) * wb.astype(np.float64)
     got = wl.bf16_bits_to_f32(ref.scale_input(a, w)).astype(np.float64)
     assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact))
+
+
+# --------------------------------------------------- all-gather / reduce-scatter
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (2, 24), (5, 8)])
+def test_agrs_route_equals_two_stage_combine_of_the_all_to_all_route(cfg, T):
+    """Two different routes, written independently (rank-major loops over every
+    gathered token vs per-slot partials of the dispatched rows), give the same bits
+    with identity experts: each is a bf16 partial per destination rank summed over
+    ranks in ascending order."""
+    x = wl.make(wl.spec(cfg, T=T) if T else wl.spec(cfg))
+    s = x.spec
+    m = ref.dispatch_meta(s.W, s.E, s.K, s.T, x.topk_ids, x.topk_weights, x.num_tokens)
+    rows = ref.dispatch_rows(m, x.a1)
+    for f32 in (False, True):
+        agrs, err = ref.agrs(s.W, s.E, s.K, s.T, x.a1, x.topk_ids, x.topk_weights, x.num_tokens, f32)
+        assert err == 0
+        assert np.array_equal(agrs, ref.combine_pagemode(m, rows, out_f32=f32))
+
+
+def test_agrs_one_rank_is_the_single_fold():
+    x = wl.make(wl.spec(2, W=1, E=8, T=40))
+    s = x.spec
+    m = ref.dispatch_meta(s.W, s.E, s.K, s.T, x.topk_ids, x.topk_weights)
+    rows = ref.dispatch_rows(m, x.a1)
+    agrs, _ = ref.agrs(s.W, s.E, s.K, s.T, x.a1, x.topk_ids, x.topk_weights)
+    assert np.array_equal(agrs, ref.combine(m, x.topk_weights, rows))
+    # identity experts with weights summing to one reproduce a1 on routed tokens
+    routed = (x.topk_ids.reshape(-1, s.K) >= 0).any(axis=1)
+    assert np.array_equal(agrs[routed], x.a1.reshape(-1, s.h)[routed])
+
+
+def test_agrs_drops_bad_pairs_like_the_router():
+    W, E, K, T = 2, 4, 3, 2
+    ids = np.array([[[0, 9, -3], [1, 1, 2]], [[-1, -1, -1], [3, 0, -2]]], np.int32)
+    w = np.full((W, T, K), 0.25, np.float32)
+    a1 = wl.f32_to_bf16_bits(np.random.default_rng(1).standard_normal((W, T, 16), dtype=np.float32))
+    out, err = ref.agrs(W, E, K, T, a1, ids, w, out_f32=True)
+    assert err & ref.ERR_EXPERT_ID and err & ref.ERR_DUPLICATE
+    x = wl.bf16_bits_to_f32(a1).reshape(W * T, 16)
+    # token (0,0): only id 0 kept -> 0.25 x; token (0,1): ids 1 and 2 kept (on ranks 0 and 1)
+    assert np.array_equal(out[0], wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(0.25 * x[0])))
+    assert (out[2] == 0).all()
