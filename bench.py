@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--eager", dest="graph", action="store_false",
                     help="launch every kernel from the host each step instead of replaying one "
                          "captured CUDA graph of dispatch + combine (the default)")
+    ap.add_argument("--route", default="a2a", choices=["a2a", "agrs"],
+                    help="agrs: time the all-gather / reduce-scatter route instead (auxiliary line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -98,13 +100,21 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# translation unit of each timed kernel; its hash also covers every shared header
+# and api.cu, which sets the kernel's launch shape
+KERNEL_TU = {"dispatch_fused": "move.cu", "move_fused": "move.cu", "pack": "move.cu",
+             "exchange": "move.cu", "deliver": "move.cu", "route": "route.cu",
+             "combine": "combine.cu", "combine_two_stage": "combine.cu", "zero_pad": "combine.cu"}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_ep_route_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, n), "rb") as f:
-                h.update(f.read())
+    names = sorted(n for n in os.listdir(csrc)
+                   if n.endswith(".cuh") or n in (KERNEL_TU[kernel], "api.cu"))
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -113,7 +123,7 @@ def traffic_for(kernel: str, cfg: int):
     on the current kernel sources (else None)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
@@ -430,6 +440,104 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def agrs_bytes(x: wl.Workload):
+    """Algorithmic bytes of one all-gather / reduce-scatter step with identity
+    experts: the gather reads each valid token row (and its ids and weights)
+    once and writes it to all W ranks; each rank reads a gathered row only when
+    one of its experts is among the token's kept pairs, reads every gathered
+    id/weight row, and writes one expert-output row per gathered token; the
+    reduce-scatter reads the W expert-output rows of each valid token and
+    writes every output row."""
+    s = x.spec
+    ids = x.topk_ids
+    live = np.arange(s.T)[None, :] < x.num_tokens[:, None]
+    n_tok = int(live.sum())
+    kept = (ids >= 0) & live[:, :, None]          # the drawn ids are distinct and < E
+    dest = np.where(kept, ids // s.e_local, -1).reshape(-1, s.K)
+    n_local_rows = sum(len(set(r[r >= 0].tolist())) for r in dest)
+    bx, bm = 2 * s.h, 8 * s.K
+    gather = (bx + bm) * n_tok * (1 + s.W)
+    experts = s.W * n_tok * bm + n_local_rows * bx + s.W * n_tok * bx
+    reduce = s.W * n_tok * bx + s.W * s.T * bx
+    return {"gather": gather, "experts": experts, "reduce_scatter": reduce}, n_local_rows
+
+
+def run_agrs(args):
+    import torch
+
+    from combine_ep_route_gb300 import EpConfig, agrs, alloc_agrs_buffers
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = wl.make(workload_spec(args))
+    s = x.spec
+    cfg = EpConfig(s.W, s.E, s.K, s.T, s.h)
+    a1 = torch.from_numpy(x.a1.view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(x.topk_ids).to(dev)
+    w = torch.from_numpy(x.topk_weights).to(dev)
+    nt = torch.from_numpy(x.num_tokens).to(dev)
+    buf = alloc_agrs_buffers(cfg, dev)
+    y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        agrs(cfg, a1, ids, w, num_tokens=nt, buffers=buf, out=y)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(buf.status.item()) != 0:
+        raise SystemExit(f"device status {int(buf.status.item())}")
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        step = graph.replay
+        for _ in range(3):
+            flush.zero_()
+            step()
+    n = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(buf.status.item()) != 0:
+        raise SystemExit(f"device status {int(buf.status.item())} after the timed region")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / n
+    parts, n_local_rows = agrs_bytes(x)
+    total = sum(parts.values())
+    peak, peak_src = measured_peaks()
+    n_tok = int(x.num_tokens.sum())
+    achieved = total / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": n_tok / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": n,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "route": "agrs",
+        "config": {"workload": s.name, "W": s.W, "E": s.E, "top_k": s.K, "tokens_per_rank": s.T,
+                   "hidden": s.h, "route": "all-gather / experts / reduce-scatter",
+                   "launch": "cuda graph replay" if args.graph else "stream", "out_dtype": "bf16",
+                   "experts": "identity", "l2": "flushed: 256 MiB write before every step"},
+        "alg_bytes_per_step": parts,
+        "counts": {"tokens": n_tok, "rank_rows_with_local_experts": n_local_rows},
+        "roofline": {"kernel": "agrs step (gather + experts + reduce-scatter)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} hbm_gbs",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None},
+        "gpu_launches": 3 * n,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(ctx, x, dev, out, n, stream, combine=None):
     """Same metric through the public API from pinned host buffers. Every step
     copies its own inputs host->device, dispatches, combines and copies its
@@ -497,6 +605,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.route == "agrs":
+        run_agrs(args)
     else:
         run_ours(args)
 

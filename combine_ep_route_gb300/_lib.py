@@ -85,6 +85,11 @@ class EpRouteOutputsC(C.Structure):
                 ("recv_row", C.c_void_p), ("expert_num_tokens", C.c_void_p), ("status", C.c_void_p)]
 
 
+class EpAgrsBuffersC(C.Structure):
+    _fields_ = [("x_g", C.c_void_p), ("ids_g", C.c_void_p), ("w_g", C.c_void_p), ("y", C.c_void_p),
+                ("status", C.c_void_p)]
+
+
 # name -> (restype, argtypes); mirrors include/ep.h one to one
 SIGNATURES = {
     "ep_capacities": (C.c_int, [C.POINTER(EpConfigC), C.POINTER(C.c_int32), C.POINTER(C.c_int32),
@@ -106,6 +111,8 @@ SIGNATURES = {
     "ep_kernel_times": (C.c_int, [C.c_void_p, C.POINTER(EpKernelTimesC)]),
     "ep_route_static": (C.c_int, [C.POINTER(EpConfigC), C.c_void_p, C.c_void_p, C.c_void_p,
                                   C.POINTER(EpRouteOutputsC), C.c_void_p]),
+    "ep_agrs": (C.c_int, [C.POINTER(EpConfigC), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                          C.POINTER(EpAgrsBuffersC), C.c_int32, C.c_void_p, C.c_void_p]),
 }
 
 _lib = None

@@ -235,3 +235,62 @@ class EpContext:
             out["send_x"] = view(m.send_x, W * W * T * rb, torch.uint8, (W, W, T, rb))
             out["recv_x"] = view(m.recv_x, W * W * T * rb, torch.uint8, (W, W, T, rb))
         return out
+
+
+# ------------------------------------------------- all-gather / reduce-scatter
+
+@dataclass
+class AgrsBuffers:
+    """Device buffers of ``ep_agrs`` (see ep_agrs_buffers_t)."""
+    x_g: torch.Tensor      # [W, W*Tm, h] bf16: every rank's gathered token rows
+    ids_g: torch.Tensor    # [W, W*Tm, K] int32
+    w_g: torch.Tensor      # [W, W*Tm, K] float32
+    y: torch.Tensor        # [W, W*Tm, h] bf16: each rank's expert output per gathered token
+    status: torch.Tensor   # [1] int32: first device-side EP_ERR_* of the last call, 0 if none
+
+    def to_c(self) -> L.EpAgrsBuffersC:
+        b = L.EpAgrsBuffersC()
+        b.x_g, b.ids_g, b.w_g = self.x_g.data_ptr(), self.ids_g.data_ptr(), self.w_g.data_ptr()
+        b.y, b.status = self.y.data_ptr(), self.status.data_ptr()
+        return b
+
+
+def alloc_agrs_buffers(cfg: EpConfig, device) -> AgrsBuffers:
+    W, T, K, h = cfg.W, cfg.max_tokens, cfg.top_k, cfg.hidden
+    dev = torch.device(device)
+    return AgrsBuffers(
+        x_g=torch.empty(W, W * T, h, dtype=torch.bfloat16, device=dev),
+        ids_g=torch.empty(W, W * T, K, dtype=torch.int32, device=dev),
+        w_g=torch.empty(W, W * T, K, dtype=torch.float32, device=dev),
+        y=torch.empty(W, W * T, h, dtype=torch.bfloat16, device=dev),
+        status=torch.zeros(1, dtype=torch.int32, device=dev))
+
+
+def agrs(cfg: EpConfig, a1: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+         num_tokens: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.bfloat16,
+         buffers: Optional[AgrsBuffers] = None, out: Optional[torch.Tensor] = None,
+         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The all-gather / reduce-scatter route with identity experts (``ep_agrs``):
+    returns out [W, Tm, h] in ``out_dtype``. Device-side errors land in
+    ``buffers.status`` (read it after synchronising)."""
+    W, T, K, h = cfg.W, cfg.max_tokens, cfg.top_k, cfg.hidden
+    dev = a1.device
+    _need(a1, "a1", torch.bfloat16, (W, T, h), dev)
+    _need(topk_ids, "topk_ids", torch.int32, (W, T, K), dev)
+    _need(topk_weights, "topk_weights", torch.float32, (W, T, K), dev)
+    if num_tokens is not None:
+        _need(num_tokens, "num_tokens", torch.int32, (W,), dev)
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be bfloat16 or float32")
+    if buffers is None:
+        buffers = alloc_agrs_buffers(cfg, dev)
+    if out is None:
+        out = torch.empty(W, T, h, dtype=out_dtype, device=dev)
+    _need(out, "out", out_dtype, (W, T, h), dev)
+    L.check(L.lib().ep_agrs(C.byref(cfg.to_c()),
+                            num_tokens.data_ptr() if num_tokens is not None else None,
+                            a1.data_ptr(), topk_ids.data_ptr(), topk_weights.data_ptr(),
+                            C.byref(buffers.to_c()),
+                            L.EP_F32 if out_dtype == torch.float32 else L.EP_BF16,
+                            out.data_ptr(), _stream_ptr(stream)), "ep_agrs")
+    return out

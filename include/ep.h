@@ -347,6 +347,64 @@ typedef struct ep_route_outputs {
 int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens, const int32_t *topk_ids,
                     const float *topk_weights, const ep_route_outputs_t *out, void *stream);
 
+/*
+ * Buffers of ep_agrs, all device memory owned by the caller.
+ *   x_g    [W(d)][W*Tm][h] bf16  every rank's all-gathered token rows
+ *   ids_g  [W(d)][W*Tm][K] int32 every rank's all-gathered top-k ids
+ *   w_g    [W(d)][W*Tm][K] float every rank's all-gathered top-k weights
+ *   y      [W(d)][W*Tm][h] bf16  each rank's expert output for every gathered token
+ *   status [1] int32 or NULL     cleared at the start of the call, then set to the
+ *                                first device-side EP_ERR_* (bad or repeated id,
+ *                                num_tokens out of range) if any
+ * Row (s*Tm + t) of a rank's block belongs to token t of rank s; rows of tokens
+ * at or past num_tokens[s] are neither written nor read.
+ */
+typedef struct ep_agrs_buffers {
+    void *x_g;
+    int32_t *ids_g;
+    float *w_g;
+    void *y;
+    int32_t *status;
+} ep_agrs_buffers_t;
+
+/*
+ * ep_agrs -- the all-gather / reduce-scatter route of vLLM's AgRsAll2AllManager
+ * (page device_communicators/all2all: its `dispatch` gathers every rank's
+ * hidden states, top-k weights and top-k ids to every rank with all_gatherv;
+ * its `combine` hands each rank back its own tokens with reduce_scatterv),
+ * with identity experts between the two, for comparison with the all-to-all
+ * route of ep_dispatch / ep_combine. It uses no context; three kernels run on
+ * `stream`:
+ *   1. all-gather: x_g[d][s*Tm+t] = a1[s][t] for every rank d, and the same for
+ *      ids and weights, for each token t < num_tokens[s];
+ *   2. experts, on each rank d (the fused-MoE step with an expert map): y[d][g]
+ *      = bf16 of the fp32 fold, in top-k order, of w_k * x_g over the token's
+ *      kept pairs whose expert lives on d (id / e_local == d), zero if none.
+ *      Pairs are kept by ep_dispatch's rule: negative ids dropped, ids >= E
+ *      and repeats of an id in a row dropped and reported;
+ *   3. reduce-scatter: out[s][t] = the sum over d = 0..W-1, ascending, of
+ *      y[d][s*Tm+t] in out_dtype (EP_BF16: each sum rounded to bf16; EP_F32:
+ *      fp32 sums); zero for t >= num_tokens[s].
+ * With identity experts the result equals ep_combine_two_stage after an
+ * ep_dispatch of the same inputs, bit for bit: both sum one bf16 partial per
+ * destination rank, ranks ascending.
+ *
+ * Inputs: num_tokens [W] int32 device or NULL (every rank holds max_tokens);
+ * a1 [W][Tm][h] bf16, topk_ids and topk_weights [W][Tm][K] (device, as for
+ * ep_dispatch); out [W][Tm][h] out_dtype (device). a1, x_g, y and out 16-byte
+ * aligned. cfg->x_dtype must be EP_BF16; EP_FLAG_WEIGHT_ON_INPUT is refused;
+ * the other flags and the extra payloads do not apply to this route and are
+ * ignored. Sizes: W * W * max_tokens * hidden / 8 < 2^31; x_g and y take
+ * 2 * W^2 * max_tokens * hidden bytes each -- W times the token bytes, which is
+ * why the route suits small W.
+ *
+ * Host-side errors: EP_ERR_INVALID_ARG (bad config, dtype, flag, size, null or
+ * misaligned pointer), EP_ERR_CUDA. Device-side errors go to buf->status.
+ */
+int ep_agrs(const ep_config_t *cfg, const int32_t *num_tokens, const void *a1,
+            const int32_t *topk_ids, const float *topk_weights, const ep_agrs_buffers_t *buf,
+            int32_t out_dtype, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

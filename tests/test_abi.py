@@ -204,3 +204,27 @@ def test_error_strings(lib):
         s = lib.ep_error_string(code).decode()
         assert s and s != "unknown status"
     assert lib.ep_error_string(-100).decode() == "unknown status"
+
+
+def test_agrs_host_checks(lib):
+    """ep_agrs refuses what it cannot run before touching any GPU."""
+    p = C.c_void_p(FAKE_WS)
+    b = L.EpAgrsBuffersC(FAKE_WS, FAKE_WS, FAKE_WS, FAKE_WS, None)
+
+    def call(c=None, a1=p, ids=p, w=p, buf=b, dt=L.EP_BF16, out=p):
+        return lib.ep_agrs(C.byref(c if c is not None else cfg(W=4, E=16, K=4, T=64, h=512)), None,
+                           a1, ids, w, C.byref(buf) if buf is not None else None, dt, out, None)
+
+    assert call(c=cfg(W=3, E=16)) == L.EP_ERR_INVALID_ARG                 # E % W != 0
+    assert call(c=cfg(W=4, E=16, K=4, T=64, h=512, x_dtype=L.EP_FP8)) == L.EP_ERR_INVALID_ARG
+    assert call(c=cfg(W=4, E=16, K=1, T=64, h=512,
+                      flags=L.EP_FLAG_WEIGHT_ON_INPUT)) == L.EP_ERR_INVALID_ARG
+    assert call(dt=3) == L.EP_ERR_INVALID_ARG
+    assert call(a1=None) == L.EP_ERR_INVALID_ARG
+    assert call(out=None) == L.EP_ERR_INVALID_ARG
+    assert call(buf=None) == L.EP_ERR_INVALID_ARG
+    assert call(buf=L.EpAgrsBuffersC(FAKE_WS, None, FAKE_WS, FAKE_WS, None)) == L.EP_ERR_INVALID_ARG
+    assert call(a1=C.c_void_p(FAKE_WS + 8)) == L.EP_ERR_INVALID_ARG      # rows need 16-byte alignment
+    assert call(buf=L.EpAgrsBuffersC(FAKE_WS, FAKE_WS, FAKE_WS, FAKE_WS + 4, None)) == L.EP_ERR_INVALID_ARG
+    # W^2 * Tm * h / 8 work items must stay below 2^31
+    assert call(c=cfg(W=64, E=64, K=8, T=8192, h=512)) == L.EP_ERR_INVALID_ARG
