@@ -51,6 +51,7 @@ EP_OPT_COMBINE_CTAS_PER_SM = 7
 EP_OPT_MOVE_CHUNK_BYTES = 8
 EP_OPT_MOVE_MAX_STAGES = 9
 EP_OPT_FUSED_DISPATCH = 10
+EP_OPT_ROUTE_CTAS = 11
 
 (EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD,
  EP_K_COMBINE_TWO_STAGE, EP_K_DISPATCH_FUSED) = range(9)

@@ -118,6 +118,7 @@ struct ep_ctx {
     int fault_skip;
     int combine_ctas_per_sm;
     int fused_dispatch;      // routing and row movement in one persistent launch
+    int route_ctas;          // CTAs of that launch that route (0 = all)
     int move_chunk_target;   // bytes; 0 = whole rows
     int move_max_stages;
     // counters and event timing
@@ -269,6 +270,7 @@ void build_move(ep_ctx *c, int mode, const void *a1, const void *const *extra_in
     uint32_t stage_bytes;
     size_t smem;
     move_shape(c, chunks, pipes, stages, stage_bytes, smem);
+    m.pipes = pipes;
     m.stages = stages;
     m.stage_bytes = stage_bytes;
     m.chunks = chunks;
@@ -353,6 +355,7 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->fault_skip = -1;
     c->combine_ctas_per_sm = 0;   // 0 = as many as fit (occupancy)
     c->fused_dispatch = 1;
+    c->route_ctas = 0;
     c->move_chunk_target = 2048;
     c->move_max_stages = 4;
     for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
@@ -420,6 +423,10 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
         case EP_OPT_FUSED_DISPATCH:
             if (value != 0 && value != 1) return EP_ERR_INVALID_ARG;
             ctx->fused_dispatch = (int)value;
+            return EP_OK;
+        case EP_OPT_ROUTE_CTAS:
+            if (value < 0 || value > 4096) return EP_ERR_INVALID_ARG;
+            ctx->route_ctas = (int)value;
             return EP_OK;
         default: return EP_ERR_INVALID_ARG;
     }
@@ -507,16 +514,14 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     int fgrid = 0, fblock = 0;
     size_t fsmem = 0;
     if (one_launch) {
-        // routing and row movement in one persistent launch needs one CTA per SM
-        // with eight pipelines (the routing step's 256 threads); rows too large
-        // for eight pipelines' stages take the two-launch path
-        const int saved_pipes = ctx->move_pipes, saved_ctas = ctx->move_ctas_per_sm;
-        ctx->move_pipes = ep::kRouteThreads / 32;
+        // routing and row movement in one persistent launch: one CTA per SM of the
+        // routing step's 256 threads, of which the first move_pipes warps (at most
+        // eight) run pipelines
+        const int saved_ctas = ctx->move_ctas_per_sm;
         ctx->move_ctas_per_sm = 1;
         build_move(ctx, ep::MOVE_FUSED, a1, extra_in, b_a1, extra_out, fm, fgrid, fblock, fsmem);
-        ctx->move_pipes = saved_pipes;
         ctx->move_ctas_per_sm = saved_ctas;
-        one_launch = fblock == ep::kRouteThreads;
+        one_launch = fblock <= ep::kRouteThreads;
     }
     if (one_launch) {
         fm.wait_tiles = 1;
@@ -524,6 +529,7 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         fm.tile_flag = rp.tile_flag;
         fm.tiles_per_rank = L.tiles_per_rank;
         fm.div_tm = ep::make_fastdiv((uint32_t)cf.max_tokens);
+        rp.route_ctas = ctx->route_ctas;
         KernelTimer tm(ctx, EP_K_DISPATCH_FUSED, st);
         if (ep::launch_dispatch_fused(rp, fm, ctx->num_sms, fsmem, st) != cudaSuccess) return EP_ERR_CUDA;
     } else {

@@ -29,7 +29,8 @@ struct DevHeader {
     uint32_t done;        // routing tiles finished in this launch
     uint32_t epoch;       // look-back epoch of the running launch; the last tile advances it
     uint32_t move_next;   // next row-mover unit handed out (fused dispatch; reset at the end)
-    uint32_t pad[58];
+    uint32_t routers;     // CTAs of the fused dispatch that asked to route (reset at the end)
+    uint32_t pad[57];
 };
 static_assert(sizeof(DevHeader) == 256, "header is one aligned block");
 
@@ -55,6 +56,7 @@ struct RouteParams {
     int32_t *expert_num_tokens;
     uint64_t wait_limit_ns;
     int32_t fault_skip_tile;
+    int32_t route_ctas;          // fused dispatch: CTAs that route (the first to arrive); 0 = all
     int32_t vec_ids;             // ids and weights 16-byte aligned: vector loads allowed
     int32_t vec_recv;            // S % 4 == 0 and recv_* 16-byte aligned: vector row stores
     int32_t unit_weights;        // weights applied on input: carry 1.0 instead of w
@@ -98,6 +100,7 @@ struct MoveParams {
     int n_tokens;                       // W*Tm
     int n_rows;                         // E*Ecap rows of the batched layout
     int n_slots;                        // W*W*Tm send-buffer rows
+    int pipes;                          // warps of a CTA that run a pipeline (the rest idle)
     int stages;                         // stages per pipeline
     uint32_t stage_bytes;
     DevHeader *hdr;

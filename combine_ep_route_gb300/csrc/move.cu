@@ -124,7 +124,7 @@ template <int MODE>
 __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, uint32_t epoch) {
     constexpr int kStash = kMaxDst + 3;   // per stage: src, count, destinations, chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int P = blockDim.x >> 5;
+    const int P = p.pipes;
     const int NS = p.stages;
     const size_t stage_region = (size_t)P * NS * p.stage_bytes;
     uint8_t *stages = smem + (size_t)warp * NS * p.stage_bytes;
@@ -223,8 +223,11 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     int nxt_src = -1, nxt_dst = -1;   // metadata of the next unit to load
     if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
 
-    // Load the warp's unit i (the next one in order) into stage i % NS and
-    // prefetch the metadata of unit i + 1.
+    // Load the warp's unit i (the next one in order) into stage i % NS, then
+    // fetch the metadata of unit i + 1 while that load is in flight (the fetch
+    // is one or more L2 round trips: a tile flag, the token's pair rows, and in
+    // the dynamic case the unit counter). Chunks of one token share metadata,
+    // so it is fetched once per token.
     auto issue = [&](int i) {
         const int st = i % NS;
         int32_t *sh = stash + st * kStash;
@@ -232,11 +235,10 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
         const uint32_t m = __ballot_sync(0xffffffffu, has);
         if (has) sh[2 + __popc(m & lanemask_lt())] = nxt_dst;
         const int src = nxt_src;
-        const int c = nxt_u % C;
-        if (lane == 0) sh[kMaxDst + 2] = c;
-        nxt_u = unit_at(i + 1);
-        if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
+        const int row_unit = nxt_u / C;
+        const int c = nxt_u - row_unit * C;
         if (lane == 0) {
+            sh[kMaxDst + 2] = c;
             sh[0] = m ? src : -1;
             sh[1] = __popc(m);
             uint64_t *bar = &bars[st];
@@ -258,6 +260,9 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
                 mbar_arrive(bar);   // empty unit: complete the phase with no transfer
             }
         }
+        nxt_u = unit_at(i + 1);
+        if (nxt_u >= 0 && nxt_u / C != row_unit)
+            unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
         __syncwarp();
     };
 
@@ -318,23 +323,30 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
     move_body<MODE>(p, smem, 0u);
 }
 
-// Routing and the fused row movement in one persistent launch. Every CTA first
-// takes routing tiles by ticket until none is left, then moves rows; a unit
-// waits only for its own token's tile, so movement starts while later tiles
-// are still being routed. No deadlock: a unit waits only on a tile some
-// running CTA already owns (all tickets are taken before any CTA moves rows),
-// and tiles wait only on tiles with smaller tickets. The last CTA to finish
-// rearms the ticket and advances the look-back epoch, as the routing kernel does.
+// Routing and the fused row movement in one persistent launch. The first
+// rp.route_ctas CTAs to arrive (all of them when it is 0) are routers: they
+// take routing tiles by ticket until none is left, then join the others in
+// moving rows with their first mp.pipes warps (the rest are done). A unit
+// waits only for its own token's tile, so movement starts as soon as the first
+// tiles are out, and routers that work through the tiles in ticket order stay
+// ahead of the movers, which take tokens in roughly ascending order. No
+// deadlock: every tile is routed by a router, a router is running from the
+// moment it is elected, routers never wait on movers, and a tile waits only on
+// tiles with smaller tickets. The last CTA to finish rearms the counters and
+// advances the look-back epoch, as the routing kernel does.
 template <int KT>
 __global__ void __launch_bounds__(256) dispatch_fused_kernel(const RouteParams rp, const MoveParams mp) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_q;
+    __shared__ int s_q, s_router;
     __shared__ uint32_t s_epoch;
     const int tid = threadIdx.x;
-    if (tid == 0) s_epoch = ld_acquire_u32(&rp.hdr->epoch) & 0x3FFFFFFFu;
+    if (tid == 0) {
+        s_epoch = ld_acquire_u32(&rp.hdr->epoch) & 0x3FFFFFFFu;
+        s_router = rp.route_ctas <= 0 || (int)atomicAdd(&rp.hdr->routers, 1u) < rp.route_ctas;
+    }
     __syncthreads();
     const uint32_t epoch = s_epoch;
-    for (;;) {
+    while (s_router) {
         if (tid == 0) s_q = (int)atomicAdd(&rp.hdr->ticket, 1u);
         __syncthreads();
         const int q = s_q;
@@ -345,13 +357,14 @@ __global__ void __launch_bounds__(256) dispatch_fused_kernel(const RouteParams r
     // the mover's bulk copies (async proxy)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    move_body<MOVE_FUSED>(mp, smem, epoch);   // mp.wait_tiles is set by the launcher
+    if ((tid >> 5) < mp.pipes) move_body<MOVE_FUSED>(mp, smem, epoch);   // mp.wait_tiles is set by the launcher
     __syncthreads();
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(&rp.hdr->done, 1u) == gridDim.x - 1) {
             atomicExch(&rp.hdr->ticket, 0u);
             atomicExch(&rp.hdr->move_next, 0u);
+            atomicExch(&rp.hdr->routers, 0u);
             atomicExch(&rp.hdr->done, 0u);
             atomicExch(&rp.hdr->epoch, (epoch + 1u) & 0x3FFFFFFFu);
         }

@@ -257,7 +257,9 @@ const char *ep_error_string(int code);
 #define EP_OPT_KERNEL_TIMING 2   /* 1: record CUDA events around every kernel */
 #define EP_OPT_PDL 3             /* 1: programmatic dependent launch between kernels (default 0) */
 #define EP_OPT_MOVE_CTAS_PER_SM 4 /* row-mover CTAs per SM (default 1) */
-#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 8) */
+#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 8); in the
+                                    one-launch fused dispatch, the warps of its 256 that move
+                                    rows once routing is done */
 #define EP_OPT_FAULT_SKIP_PUBLISH 6 /* test hook: the routing tile with this ticket never
                                        publishes, so its successors' waits run out and
                                        report EP_ERR_TIMEOUT; -1 (default) = off */
@@ -267,6 +269,9 @@ const char *ep_error_string(int code);
 #define EP_OPT_MOVE_MAX_STAGES 9  /* row-mover stages per pipeline, at most (2..32, default 4) */
 #define EP_OPT_FUSED_DISPATCH 10  /* 1 (default): the fused path routes and moves rows in one
                                      persistent launch, movement starting as tiles finish */
+#define EP_OPT_ROUTE_CTAS 11      /* one-launch fused dispatch: how many CTAs route (the first
+                                     to start; the others move rows from the outset);
+                                     0 = every CTA routes first (0..4096) */
 
 /* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
 int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);

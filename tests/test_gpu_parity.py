@@ -213,6 +213,9 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     {L.EP_OPT_MOVE_CHUNK_BYTES: 0},
     {L.EP_OPT_FUSED_DISPATCH: 0},
     {L.EP_OPT_FUSED_DISPATCH: 0, L.EP_OPT_PDL: 1},
+    {L.EP_OPT_ROUTE_CTAS: 1},
+    {L.EP_OPT_ROUTE_CTAS: 3, L.EP_OPT_MOVE_PIPES: 4},
+    {L.EP_OPT_ROUTE_CTAS: 4096},
 ])
 @pytest.mark.parametrize("path", ["fused", "sendbuf"])
 def test_launch_options_do_not_change_results(dev, opts, path):
