@@ -194,9 +194,12 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     // kStaticUnits units by stride and the rest in batches of kUnitBatch grabbed
     // from a launch-wide counter, so a warp that starts late (after routing a
     // tile in the same launch) takes fewer units, while small problems never
-    // touch the counter. Called with i growing by at most one per new value.
+    // touch the counter. The last two rounds are grabbed one unit at a time, so
+    // the warps finish within about one unit of each other. Called with i
+    // growing by at most one per new value.
     constexpr int kStaticUnits = 2, kUnitBatch = 4;
     const bool dyn = p.dynamic_units != 0;
+    const int tail_from = n_work - 2 * kUnitBatch * stride;
     int seq_base = 0, seq_len = 0, seq_i0 = kStaticUnits;
     auto unit_at = [&](int i) -> int {
         if (!dyn || i < kStaticUnits) {
@@ -205,8 +208,10 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
         }
         while (i >= seq_i0 + seq_len) {
             if (seq_len < 0) return -1;   // the counter ran out
+            // seq_base (the warp's last batch) stands in for the counter
+            const int want = seq_base >= tail_from ? 1 : kUnitBatch;
             int b = 0;
-            if (lane == 0) b = (int)atomicAdd(&p.hdr->move_next, (uint32_t)kUnitBatch);
+            if (lane == 0) b = (int)atomicAdd(&p.hdr->move_next, (uint32_t)want);
             b = __shfl_sync(0xffffffffu, b, 0) + kStaticUnits * stride;
             seq_i0 += seq_len;
             if (b >= n_work) {
@@ -214,7 +219,7 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
                 return -1;
             }
             seq_base = b;
-            seq_len = min(kUnitBatch, n_work - b);
+            seq_len = min(want, n_work - b);
         }
         return seq_base + (i - seq_i0);
     };
@@ -335,23 +340,31 @@ __global__ void __launch_bounds__(256) move_kernel(const MoveParams p) {
 // tiles with smaller tickets. The last CTA to finish rearms the counters and
 // advances the look-back epoch, as the routing kernel does.
 template <int KT>
-__global__ void __launch_bounds__(256) dispatch_fused_kernel(const RouteParams rp, const MoveParams mp) {
+__global__ void __launch_bounds__(256, 2) dispatch_fused_kernel(const RouteParams rp, const MoveParams mp) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_q, s_router;
+    __shared__ int s_q;
     __shared__ uint32_t s_epoch;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        s_epoch = ld_acquire_u32(&rp.hdr->epoch) & 0x3FFFFFFFu;
-        s_router = rp.route_ctas <= 0 || (int)atomicAdd(&rp.hdr->routers, 1u) < rp.route_ctas;
+        // The epoch was last written by the previous launch (ordered before this
+        // one by the launch boundary) and is written in this one only after every
+        // CTA has read it: a relaxed load suffices, and the first ticket need not
+        // wait for it.
+        const uint32_t e = ld_relaxed_u32(&rp.hdr->epoch);
+        const bool router = rp.route_ctas <= 0 || (int)atomicAdd(&rp.hdr->routers, 1u) < rp.route_ctas;
+        s_q = router ? (int)atomicAdd(&rp.hdr->ticket, 1u) : rp.num_tiles;
+        s_epoch = e & 0x3FFFFFFFu;
     }
     __syncthreads();
     const uint32_t epoch = s_epoch;
-    while (s_router) {
-        if (tid == 0) s_q = (int)atomicAdd(&rp.hdr->ticket, 1u);
-        __syncthreads();
+    for (;;) {
         const int q = s_q;
         if (q >= rp.num_tiles) break;   // uniform across the CTA
+        // route_tile begins with a barrier, so every thread has read s_q before
+        // thread 0 replaces it below
         route_tile<KT>(rp, q, epoch, reinterpret_cast<uint32_t *>(smem));
+        if (tid == 0) s_q = (int)atomicAdd(&rp.hdr->ticket, 1u);
+        __syncthreads();
     }
     // shared memory now changes hands from the routing step (generic writes) to
     // the mover's bulk copies (async proxy)

@@ -18,8 +18,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
         // The epoch lives in device memory and only the launch's last CTA
         // advances it (after every CTA has read it), so every tile of one launch
         // reads the same value, and a replayed launch (a CUDA graph) gets a
-        // fresh one without any host involvement.
-        s_epoch = ld_acquire_u32(&p.hdr->epoch) & 0x3FFFFFFFu;
+        // fresh one without any host involvement. The previous launch's write is
+        // ordered before this launch by the launch boundary: a relaxed load.
+        s_epoch = ld_relaxed_u32(&p.hdr->epoch) & 0x3FFFFFFFu;
     }
     __syncthreads();
     // Every routing CTA is resident once it gets here, so a dependent kernel

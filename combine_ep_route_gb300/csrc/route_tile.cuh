@@ -25,8 +25,9 @@
 //      inclusive prefixes of up to 32 predecessor tiles per step into the tile's
 //      exclusive prefix; the destination counters restart at every rank;
 //   4. one thread per (token, k) pair writes the pair's row, weight and slot
-//      (coalesced); the first pair of a token on each destination also writes
-//      that destination's received-slot row with 16-byte vector stores.
+//      (coalesced) and the tile publishes them; then the first pair of a token
+//      on each destination writes that destination's received-slot row with
+//      16-byte vector stores.
 // Every wait is bounded: past the limit the tile records EP_ERR_TIMEOUT and
 // finishes with what it has, so no launch can hang.
 #pragma once
@@ -49,7 +50,7 @@ inline size_t route_smem_bytes(int n_ctr, int top_k) {
 }
 
 // Tile flag states (low two bits; the epoch is above them): 1 = aggregate
-// published, 2 = inclusive prefix published, 3 = prefix and outputs published.
+// published, 2 = inclusive prefix published, 3 = prefix and pair outputs published.
 constexpr uint32_t kFlagAgg = 1u, kFlagIncl = 2u, kFlagDone = 3u;
 constexpr uint32_t kFlagTimeout = 4u;   // what a wait returns when its limit runs out
 
@@ -75,8 +76,10 @@ __device__ __forceinline__ uint32_t wait_tile_flag(const uint32_t *f, uint32_t e
 
 // One routing tile (ticket q) with the whole CTA (kRouteThreads threads), using
 // shared memory sm (route_smem_bytes). epoch: this launch's look-back epoch.
-// When it returns, the tile's outputs are written and published: its flag
-// reads `epoch << 2 | 3` (3 = outputs done; the look-back treats 2 and 3 alike).
+// When it returns, the tile's outputs are written, and its flag reads
+// `epoch << 2 | 3` (3 = the pair outputs are published: pair_row, pair_w and
+// pair_send; the received-slot rows and counts are written after it and are
+// for later launches; the look-back treats 2 and 3 alike).
 // KT: top_k rounded up to a power of two (compile-time loop bounds).
 template <int KT>
 __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epoch, uint32_t *sm) {
@@ -99,20 +102,18 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
     const int W = p.W, K = p.K, e_local = p.e_local;
     const int s = q / p.tiles_per_rank;
     const int t0 = (q - s * p.tiles_per_rank) * kRouteTile;   // first token of the tile
-    int T = p.num_tokens ? p.num_tokens[s] : p.Tm;
-    if (T < 0 || T > p.Tm) {
-        if (tid == 0 && q % p.tiles_per_rank == 0) raise_error(p.hdr, EP_ERR_CAPACITY);
-        T = T < 0 ? 0 : p.Tm;
-    }
+    // the rank's token count and the tile's ids are loaded together: ids of every
+    // token below max_tokens are read, and those at or past the count dropped after
+    const int T_in = p.num_tokens ? __ldg(p.num_tokens + s) : p.Tm;
 
     // 1. one thread per token: load, validate, lane bitmasks
+    int ek[KT];
+    float wk[KT];
     if (tid < kRouteTile) {
         const int t = t0 + tid;
-        const bool valid = t < T;
+        const bool inb = t < p.Tm;
         const int64_t g = (int64_t)s * p.Tm + t;
-        int ek[KT];
-        float wk[KT];
-        if (valid && KT % 4 == 0 && K == KT && p.vec_ids) {
+        if (inb && KT % 4 == 0 && K == KT && p.vec_ids) {
             const int4 *pi = reinterpret_cast<const int4 *>(p.ids + g * KT);
             const float4 *pw = reinterpret_cast<const float4 *>(p.weights + g * KT);
 #pragma unroll
@@ -125,9 +126,20 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
         } else {
 #pragma unroll
             for (int k = 0; k < KT; ++k) {
-                ek[k] = (valid && k < K) ? __ldg(p.ids + g * K + k) : -1;
-                wk[k] = (valid && k < K) ? __ldg(p.weights + g * K + k) : 0.f;
+                ek[k] = (inb && k < K) ? __ldg(p.ids + g * K + k) : -1;
+                wk[k] = (inb && k < K) ? __ldg(p.weights + g * K + k) : 0.f;
             }
+        }
+    }
+    int T = T_in;
+    if (T < 0 || T > p.Tm) {
+        if (tid == 0 && q % p.tiles_per_rank == 0) raise_error(p.hdr, EP_ERR_CAPACITY);
+        T = T < 0 ? 0 : p.Tm;
+    }
+    if (tid < kRouteTile) {
+        if (t0 + tid >= T) {
+#pragma unroll
+            for (int k = 0; k < KT; ++k) ek[k] = -1;
         }
         uint32_t keep = 0;
 #pragma unroll
@@ -180,7 +192,6 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
         for (int c = tid; c < n_ctr; c += kRouteThreads) p.tile_agg[(size_t)q * vec + c] = agg[c];
         __syncthreads();
         if (tid == 0 && publish) {
-            __threadfence();
             st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagAgg);
         }
         int pidx = q - 1;
@@ -230,20 +241,40 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
     }
     for (int c = tid; c < n_ctr; c += kRouteThreads) p.tile_incl[(size_t)q * vec + c] = excl[c] + agg[c];
     __syncthreads();
-    if (tid == 0 && publish) {
-        __threadfence();
-        st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagIncl);
-    }
+    if (tid == 0 && publish) st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagIncl);
 
-    // 4. one thread per (token, k) pair writes the pair's row, weight and send
-    // slot (coalesced). The first pair of a token on a destination also writes
-    // that destination's whole received-slot row (S columns of local id,
-    // weight and row), assembled in registers and stored as 16-byte vectors.
-    // After a timed-out wait the prefix is not trusted: the tile marks its
-    // pairs as taking no part. Every index is range-checked before it is used,
-    // so a bad prefix can never write out of bounds.
+    // 4. one thread per (token, k) pair. (a) Each pair's row, weight and send
+    // slot are written (coalesced) and published: that is all the row movers of
+    // the same launch read. (b) Then the first pair of a token on each
+    // destination writes that destination's whole received-slot row (S columns
+    // of local id, weight and row), assembled in registers and stored as
+    // 16-byte vectors, and the tile's last counters are written; later
+    // launches read those. After a timed-out wait the prefix is not trusted:
+    // the tile marks its pairs as taking no part. Every index is range-checked
+    // before it is used, so a bad prefix can never write out of bounds.
     const bool bad = s_bad != 0;
     const int rows_in_tile = min(kRouteTile, p.Tm - t0);
+    // slot of the pair's token on destination d and the pair's row in its
+    // expert; false if the pair was dropped or its position is out of range
+    auto locate = [&](int tl, int pk, int &slot, int &row) -> bool {
+        if (pk < 0 || bad) return false;
+        const int e = pk & 0xFFFF, d = pk >> 16;
+        const int tw = tl >> 5;
+        const uint32_t lt = (1u << (tl & 31)) - 1u;
+        const uint32_t *wb = bits + tw * n_ctr;
+        const int32_t *wo = woff + tw * n_ctr;
+        slot = excl[d] + wo[d] + __popc(wb[d] & lt);
+        row = excl[W + e] + wo[W + e] + __popc(wb[W + e] & lt);
+        return slot >= 0 && slot < T && row >= 0 && row < p.Ecap;
+    };
+    // true if no earlier kept pair of the token goes to the same destination
+    auto first_on_dest = [&](const int32_t *te, int k, int d) -> bool {
+        bool first = true;
+#pragma unroll
+        for (int k2 = 0; k2 < KT; ++k2)
+            if (k2 < k && te[k2] >= 0 && (te[k2] >> 16) == d) first = false;
+        return first;
+    };
     for (int pi = tid; pi < rows_in_tile * KT; pi += kRouteThreads) {
         const int tl = pi / KT, k = pi % KT;
         if (k >= K) continue;
@@ -252,80 +283,84 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
         const int pk = te[k];
         int32_t prow = -1, psend = -1;
         float pw = 0.f;
-        if (pk >= 0 && !bad) {
+        int slot = 0, row = 0;
+        if (locate(tl, pk, slot, row)) {
             const int e = pk & 0xFFFF, d = pk >> 16;
-            const int tw = tl >> 5;
-            const uint32_t lt = (1u << (tl & 31)) - 1u;
-            const uint32_t *wb = bits + tw * n_ctr;
-            const int32_t *wo = woff + tw * n_ctr;
-            const int slot = excl[d] + wo[d] + __popc(wb[d] & lt);
-            const int row = excl[W + e] + wo[W + e] + __popc(wb[W + e] & lt);
-            if (slot < 0 || slot >= T || row < 0 || row >= p.Ecap) {
-                raise_error(p.hdr, EP_ERR_STATE);
-            } else {
-                prow = e * p.Ecap + row;
-                pw = p.unit_weights ? 1.0f : sw[tl * KT + k];
-                bool first = true;   // no earlier pair of this token on d
-#pragma unroll
-                for (int k2 = 0; k2 < KT; ++k2)
-                    if (k2 < k && te[k2] >= 0 && (te[k2] >> 16) == d) first = false;
-                if (first) {
-                    psend = (s * W + d) * p.Tm + slot;
-                    // columns: the token's pairs on d in top-k order, then unused
-                    int cj[KT], cr[KT];
-                    float cw[KT];
-#pragma unroll
-                    for (int c = 0; c < KT; ++c) {
-                        cj[c] = -1;
-                        cr[c] = -1;
-                        cw[c] = 0.f;
-                    }
-                    int n = 0;
-                    const int jbase = d * e_local;
-#pragma unroll
-                    for (int k2 = 0; k2 < KT; ++k2) {
-                        const int p2 = te[k2];
-                        if (p2 >= 0 && (p2 >> 16) == d) {
-                            const int e2 = p2 & 0xFFFF;
-                            const int r2 = excl[W + e2] + wo[W + e2] + __popc(wb[W + e2] & lt);
-                            const float w2 = p.unit_weights ? 1.0f : sw[tl * KT + k2];
-#pragma unroll
-                            for (int c = 0; c < KT; ++c)
-                                if (c == n) {
-                                    cj[c] = e2 - jbase;
-                                    cr[c] = r2;
-                                    cw[c] = w2;
-                                }
-                            ++n;
-                        }
-                    }
-                    const size_t rb = ((size_t)(d * W + s) * p.Tm + slot) * p.S;
-                    if (KT >= 4 && p.vec_recv) {   // S % 4 == 0, 16-byte aligned rows
-#pragma unroll
-                        for (int c4 = 0; c4 < KT / 4; ++c4) {
-                            if (4 * c4 >= p.S) break;
-                            reinterpret_cast<int4 *>(p.recv_eloc + rb)[c4] =
-                                make_int4(cj[4 * c4], cj[4 * c4 + 1], cj[4 * c4 + 2], cj[4 * c4 + 3]);
-                            reinterpret_cast<int4 *>(p.recv_row + rb)[c4] =
-                                make_int4(cr[4 * c4], cr[4 * c4 + 1], cr[4 * c4 + 2], cr[4 * c4 + 3]);
-                            reinterpret_cast<float4 *>(p.recv_w + rb)[c4] =
-                                make_float4(cw[4 * c4], cw[4 * c4 + 1], cw[4 * c4 + 2], cw[4 * c4 + 3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < KT; ++c) {
-                            if (c >= p.S) break;
-                            p.recv_eloc[rb + c] = cj[c];
-                            p.recv_row[rb + c] = cr[c];
-                            p.recv_w[rb + c] = cw[c];
-                        }
-                    }
-                }
-            }
+            prow = e * p.Ecap + row;
+            pw = p.unit_weights ? 1.0f : sw[tl * KT + k];
+            if (first_on_dest(te, k, d)) psend = (s * W + d) * p.Tm + slot;
+        } else if (pk >= 0 && !bad) {
+            raise_error(p.hdr, EP_ERR_STATE);
         }
         p.pair_row[g * K + k] = prow;
         p.pair_w[g * K + k] = pw;
         p.pair_send[g * K + k] = psend;
+    }
+    __syncthreads();
+    if (tid == 0 && publish) st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagDone);
+
+    for (int pi = tid; pi < rows_in_tile * KT; pi += kRouteThreads) {
+        const int tl = pi / KT, k = pi % KT;
+        if (k >= K) continue;
+        const int32_t *te = sid + tl * KT;
+        const int pk = te[k];
+        int slot = 0, row = 0;
+        if (!locate(tl, pk, slot, row)) continue;
+        const int d = pk >> 16;
+        if (!first_on_dest(te, k, d)) continue;
+        // columns: the token's pairs on d in top-k order, then unused
+        const int tw = tl >> 5;
+        const uint32_t lt = (1u << (tl & 31)) - 1u;
+        const uint32_t *wb = bits + tw * n_ctr;
+        const int32_t *wo = woff + tw * n_ctr;
+        int cj[KT], cr[KT];
+        float cw[KT];
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+            cj[c] = -1;
+            cr[c] = -1;
+            cw[c] = 0.f;
+        }
+        int n = 0;
+        const int jbase = d * e_local;
+#pragma unroll
+        for (int k2 = 0; k2 < KT; ++k2) {
+            const int p2 = te[k2];
+            if (p2 >= 0 && (p2 >> 16) == d) {
+                const int e2 = p2 & 0xFFFF;
+                const int r2 = excl[W + e2] + wo[W + e2] + __popc(wb[W + e2] & lt);
+                const float w2 = p.unit_weights ? 1.0f : sw[tl * KT + k2];
+#pragma unroll
+                for (int c = 0; c < KT; ++c)
+                    if (c == n) {
+                        cj[c] = e2 - jbase;
+                        cr[c] = r2;
+                        cw[c] = w2;
+                    }
+                ++n;
+            }
+        }
+        const size_t rb = ((size_t)(d * W + s) * p.Tm + slot) * p.S;
+        if (KT >= 4 && p.vec_recv) {   // S % 4 == 0, 16-byte aligned rows
+#pragma unroll
+            for (int c4 = 0; c4 < KT / 4; ++c4) {
+                if (4 * c4 >= p.S) break;
+                reinterpret_cast<int4 *>(p.recv_eloc + rb)[c4] =
+                    make_int4(cj[4 * c4], cj[4 * c4 + 1], cj[4 * c4 + 2], cj[4 * c4 + 3]);
+                reinterpret_cast<int4 *>(p.recv_row + rb)[c4] =
+                    make_int4(cr[4 * c4], cr[4 * c4 + 1], cr[4 * c4 + 2], cr[4 * c4 + 3]);
+                reinterpret_cast<float4 *>(p.recv_w + rb)[c4] =
+                    make_float4(cw[4 * c4], cw[4 * c4 + 1], cw[4 * c4 + 2], cw[4 * c4 + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < KT; ++c) {
+                if (c >= p.S) break;
+                p.recv_eloc[rb + c] = cj[c];
+                p.recv_row[rb + c] = cr[c];
+                p.recv_w[rb + c] = cw[c];
+            }
+        }
     }
 
     // per-rank slot counts and per-expert row counts
@@ -335,13 +370,6 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
     if (q == p.num_tiles - 1)
         for (int e = tid; e < p.E; e += kRouteThreads)
             p.expert_num_tokens[e] = bad ? 0 : min(max(excl[W + e] + agg[W + e], 0), p.Ecap);
-
-    // outputs written: publish them for a consumer in the same launch
-    __syncthreads();
-    if (tid == 0 && publish) {
-        __threadfence();
-        st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagDone);
-    }
 }
 
 }  // namespace ep
