@@ -107,7 +107,8 @@ def measured_peaks():
 # and api.cu, which sets the kernel's launch shape
 KERNEL_TU = {"dispatch_fused": "move.cu", "move_fused": "move.cu", "pack": "move.cu",
              "exchange": "move.cu", "deliver": "move.cu", "route": "route.cu",
-             "combine": "combine.cu", "combine_two_stage": "combine.cu", "zero_pad": "combine.cu"}
+             "combine": "combine.cu", "combine_two_stage": "combine.cu", "zero_pad": "combine.cu",
+             "agrs_gather": "agrs.cu", "agrs_experts": "agrs.cu", "agrs_reduce": "agrs.cu"}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -523,6 +524,8 @@ def run_agrs(args):
     peak, peak_src = measured_peaks()
     n_tok = int(x.num_tokens.sum())
     achieved = total / (ms * 1e-3) / 1e9
+    tr = [traffic_for(k, args.config) for k in ("agrs_gather", "agrs_experts", "agrs_reduce")]
+    traffic = sum(tr) if all(t is not None for t in tr) else None
     line = {
         "metric": METRIC, "value": n_tok / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": n,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
@@ -536,7 +539,7 @@ def run_agrs(args):
         "counts": {"tokens": n_tok, "rank_rows_with_local_experts": n_local_rows},
         "roofline": {"kernel": "agrs step (gather + experts + reduce-scatter)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} hbm_gbs",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None},
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic},
         "gpu_launches": 3 * n,
         "clocks": clk.summary(),
     }

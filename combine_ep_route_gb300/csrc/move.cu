@@ -224,9 +224,26 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
         return seq_base + (i - seq_i0);
     };
 
-    int nxt_u = unit_at(0);
+    int nxt_u = -1;
     int nxt_src = -1, nxt_dst = -1;   // metadata of the next unit to load
-    if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
+
+    // lane 0: load source row src, chunk c, into stage st (completion on its mbarrier)
+    auto load_unit = [&](int st, int src, int c) {
+        uint64_t *bar = &bars[st];
+        uint8_t *stg = stages + (size_t)st * p.stage_bytes;
+        mbar_arrive_expect_tx(bar, cb + (c == 0 ? tail : 0u));
+        if (src_split) {
+            bulk_g2s(stg, p.src_seg[0] + (size_t)src * a1b + (size_t)c * cb, cb, bar);
+            if (c == 0)
+                for (int sg = 1; sg < p.n_seg; ++sg)
+                    bulk_g2s(stg + cb + (p.seg_off[sg] - a1b),
+                             p.src_seg[sg] + (size_t)src * p.seg_bytes[sg], p.seg_bytes[sg], bar);
+        } else {
+            const uint8_t *row = src_whole + (size_t)src * p.row_bytes;
+            bulk_g2s(stg, row + (size_t)c * cb, cb, bar);
+            if (c == 0 && tail) bulk_g2s(stg + cb, row + a1b, tail, bar);
+        }
+    };
 
     // Load the warp's unit i (the next one in order) into stage i % NS, then
     // fetch the metadata of unit i + 1 while that load is in flight (the fetch
@@ -246,24 +263,8 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
             sh[kMaxDst + 2] = c;
             sh[0] = m ? src : -1;
             sh[1] = __popc(m);
-            uint64_t *bar = &bars[st];
-            uint8_t *stg = stages + (size_t)st * p.stage_bytes;
-            if (m) {
-                mbar_arrive_expect_tx(bar, cb + (c == 0 ? tail : 0u));
-                if (src_split) {
-                    bulk_g2s(stg, p.src_seg[0] + (size_t)src * a1b + (size_t)c * cb, cb, bar);
-                    if (c == 0)
-                        for (int sg = 1; sg < p.n_seg; ++sg)
-                            bulk_g2s(stg + cb + (p.seg_off[sg] - a1b),
-                                     p.src_seg[sg] + (size_t)src * p.seg_bytes[sg], p.seg_bytes[sg], bar);
-                } else {
-                    const uint8_t *row = src_whole + (size_t)src * p.row_bytes;
-                    bulk_g2s(stg, row + (size_t)c * cb, cb, bar);
-                    if (c == 0 && tail) bulk_g2s(stg + cb, row + a1b, tail, bar);
-                }
-            } else {
-                mbar_arrive(bar);   // empty unit: complete the phase with no transfer
-            }
+            if (m) load_unit(st, src, c);
+            else mbar_arrive(&bars[st]);   // empty unit: complete the phase with no transfer
         }
         nxt_u = unit_at(i + 1);
         if (nxt_u >= 0 && nxt_u / C != row_unit)
@@ -272,6 +273,54 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     };
 
     int issued = 0;
+    if (src_split && p.wait_tiles) {
+        // Routing runs in this launch: fill the first stages before the
+        // destinations are known. A unit's source row follows from its index,
+        // so its load overlaps the wait for its routing tile; a unit that turns
+        // out to have no destination was loaded for nothing and is skipped.
+        for (; issued < NS; ++issued) {
+            const int u = unit_at(issued);
+            if (u < 0) break;
+            if (lane == 0) {
+                int32_t *sh = stash + issued * kStash;
+                const int row_unit = u / C, c = u - row_unit * C;
+                sh[0] = row_unit;
+                sh[kMaxDst + 2] = c;
+                load_unit(issued, row_unit, c);
+            }
+        }
+        __syncwarp();
+        int prev = -1, src = -1, dst = -1;
+        for (int j = 0; j < issued; ++j) {
+            int32_t *sh = stash + j * kStash;
+            const int row_unit = sh[0];
+            __syncwarp();   // every lane has read sh[0] before lane 0 rewrites it
+            if (row_unit != prev) {
+                unit_meta<MODE>(p, pre, row_unit, lane, epoch, src, dst);
+                prev = row_unit;
+            }
+            const bool has = dst >= 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, has);
+            if (has) sh[2 + __popc(m & lanemask_lt())] = dst;
+            if (lane == 0) {
+                sh[0] = m ? src : -1;
+                sh[1] = __popc(m);
+            }
+        }
+        nxt_u = unit_at(issued);
+        if (nxt_u >= 0) {
+            if (nxt_u / C == prev) {
+                nxt_src = src;
+                nxt_dst = dst;
+            } else {
+                unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
+            }
+        }
+        __syncwarp();
+    } else {
+        nxt_u = unit_at(0);
+        if (nxt_u >= 0) unit_meta<MODE>(p, pre, nxt_u / C, lane, epoch, nxt_src, nxt_dst);
+    }
     while (issued < NS && nxt_u >= 0) issue(issued++);
     int consumed = 0;
     bool ok = true;

@@ -216,6 +216,7 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     {L.EP_OPT_ROUTE_CTAS: 1},
     {L.EP_OPT_ROUTE_CTAS: 3, L.EP_OPT_MOVE_PIPES: 4},
     {L.EP_OPT_ROUTE_CTAS: 4096},
+    {L.EP_OPT_ROUTE_CTAS: 0},
 ])
 @pytest.mark.parametrize("path", ["fused", "sendbuf"])
 def test_launch_options_do_not_change_results(dev, opts, path):
