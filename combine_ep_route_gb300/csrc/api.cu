@@ -705,10 +705,9 @@ int ep_combine_two_stage(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtyp
     b.div_nvec = a.div_nvec;
     b.div_tm = a.div_tm;
     b.div_w = a.div_w;
-    const int grid = ctx->num_sms * 4;
     {
         KernelTimer tm(ctx, EP_K_COMBINE_TWO_STAGE, st);
-        if (ep::launch_combine_two_stage(a, b, out_dtype == EP_F32, grid, st) != cudaSuccess)
+        if (ep::launch_combine_two_stage(a, b, out_dtype == EP_F32, ctx->num_sms, st) != cudaSuccess)
             return EP_ERR_CUDA;
         ctx->launches[EP_K_COMBINE_TWO_STAGE]++;   // two kernels under one timer
     }

@@ -181,27 +181,39 @@ __global__ void __launch_bounds__(256) combine_partial_kernel(const PartialParam
             w[c] = __shfl_sync(0xffffffffu, my_w, from);
         }
         uint8_t *dst = p.part + (size_t)r * p.part_stride;
-        // four vectors per lane per round, so each column's loads go out together
+        // four vectors per lane per round; two columns' loads go out together, so
+        // a slot with several columns keeps twice the bytes in flight
         for (int v0 = lane; v0 < p.nvec; v0 += 128) {
             float a[4][8];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) a[u][i] = 0.f;
-            for (int c = 0; c < nv; ++c) {
-                const uint8_t *row = p.expert_out + (size_t)src[c] * row_bytes;
-                uint4 x[4];
+#pragma unroll
+            for (int c = 0; c < ST; c += 2) {
+                if (c >= nv) break;
+                const bool two = c + 1 < nv;
+                const uint8_t *row0 = p.expert_out + (size_t)src[c] * row_bytes;
+                const uint8_t *row1 = p.expert_out + (size_t)(two ? src[c + 1] : src[c]) * row_bytes;
+                uint4 x[2][4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int v = v0 + 32 * u;
-                    x[u] = v < p.nvec ? ld_stream_v4(row + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    const bool in = v < p.nvec;
+                    x[0][u] = in ? ld_stream_v4(row0 + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    x[1][u] = in && two ? ld_stream_v4(row1 + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    fold2(a[u][0], a[u][1], w[c], x[u].x);
-                    fold2(a[u][2], a[u][3], w[c], x[u].y);
-                    fold2(a[u][4], a[u][5], w[c], x[u].z);
-                    fold2(a[u][6], a[u][7], w[c], x[u].w);
+                for (int q = 0; q < 2; ++q) {
+                    if (q == 1 && !two) break;
+                    const float wc = w[c + q];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        fold2(a[u][0], a[u][1], wc, x[q][u].x);
+                        fold2(a[u][2], a[u][3], wc, x[q][u].y);
+                        fold2(a[u][4], a[u][5], wc, x[q][u].z);
+                        fold2(a[u][6], a[u][7], wc, x[q][u].w);
+                    }
                 }
             }
 #pragma unroll
@@ -237,108 +249,134 @@ __device__ __forceinline__ void add2(float &a0, float &a1, uint32_t x) {
     }
 }
 
+__device__ __forceinline__ void cmp_swap(int &a, int &b) {
+    const int lo = min(a, b), hi = max(a, b);
+    a = lo;
+    b = hi;
+}
+
+// Ascending sort of N register values: an optimal 19-exchange network for 8
+// (Knuth, TAOCP vol. 3, 5.3.4), insertion sort otherwise.
+template <int N>
+__device__ __forceinline__ void sort_ascending(int (&v)[N]) {
+    if constexpr (N == 8) {
+        cmp_swap(v[0], v[2]); cmp_swap(v[1], v[3]); cmp_swap(v[4], v[6]); cmp_swap(v[5], v[7]);
+        cmp_swap(v[0], v[4]); cmp_swap(v[1], v[5]); cmp_swap(v[2], v[6]); cmp_swap(v[3], v[7]);
+        cmp_swap(v[0], v[1]); cmp_swap(v[2], v[3]); cmp_swap(v[4], v[5]); cmp_swap(v[6], v[7]);
+        cmp_swap(v[2], v[4]); cmp_swap(v[3], v[5]);
+        cmp_swap(v[1], v[4]); cmp_swap(v[3], v[6]);
+        cmp_swap(v[1], v[2]); cmp_swap(v[3], v[4]); cmp_swap(v[5], v[6]);
+    } else {
+#pragma unroll
+        for (int i = 1; i < N; ++i)
+#pragma unroll
+            for (int k = i; k > 0; --k) cmp_swap(v[k - 1], v[k]);
+    }
+}
+
 template <int KT, bool OUT_F32>
 __global__ void __launch_bounds__(256) combine_gather_kernel(const GatherParams p) {
-    // one warp per token; its destination list is read once and broadcast
-    const int lane = threadIdx.x & 31;
-    const uint32_t n_tok = (uint32_t)p.W * p.Tm;
-    for (uint32_t g = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < n_tok;
-         g += (gridDim.x * blockDim.x) >> 5) {
+    // one thread per 16 bytes of bf16 input of one token: the token's send rows
+    // (at most one per destination rank) sorted ascending -- ascending rank --
+    // then every partial's load issued before the sum
+    for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < p.n_items;
+         idx += gridDim.x * blockDim.x) {
+        const uint32_t g = fastdiv(idx, p.div_nvec);
+        const uint32_t v = idx - g * (uint32_t)p.nvec;
         const int s = (int)fastdiv(g, p.div_tm);
-        int mine = lane < p.K ? __ldg(p.pair_send + (size_t)g * p.K + lane) : -1;
-        // the token's send rows in ascending order (= ascending destination rank)
         int sr[KT];
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
-            const int x = __shfl_sync(0xffffffffu, mine, k);
+            const int x = k < p.K ? __ldg(p.pair_send + (size_t)g * p.K + k) : -1;
             sr[k] = x < 0 ? 0x7FFFFFFF : x;
         }
+        sort_ascending<KT>(sr);
+        uint4 x[KT];
+        bool has[KT];
 #pragma unroll
-        for (int i = 1; i < KT; ++i)
-#pragma unroll
-            for (int k = i; k > 0; --k)
-                if (sr[k] < sr[k - 1]) {
-                    const int t = sr[k];
-                    sr[k] = sr[k - 1];
-                    sr[k - 1] = t;
-                }
-        int64_t rrow[KT];   // the partial row of each destination, in the rank-d block
-#pragma unroll
-        for (int k = 0; k < KT; ++k) {
-            rrow[k] = -1;
+        for (int k = 0; k < KT; ++k) {   // the partial row of each destination, in the rank-d block
+            has[k] = false;
+            x[k] = make_uint4(0u, 0u, 0u, 0u);
             if (sr[k] != 0x7FFFFFFF) {
                 const uint32_t sd = fastdiv((uint32_t)sr[k], p.div_tm);   // s * W + d
                 const int slot = (int)((uint32_t)sr[k] - sd * (uint32_t)p.Tm);
                 const int d = (int)(sd - (uint32_t)s * (uint32_t)p.W);
-                if (d >= 0 && d < p.W) rrow[k] = ((int64_t)d * p.W + s) * p.Tm + slot;
+                if (d >= 0 && d < p.W) {
+                    const size_t rrow = ((size_t)d * p.W + s) * p.Tm + slot;
+                    x[k] = ld_stream_v4(p.part + rrow * p.part_stride + (size_t)v * 16);
+                    has[k] = true;
+                }
             }
         }
-        for (int v0 = lane; v0 < p.nvec; v0 += 128) {
-            float a[4][8];
+        float a[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+        for (int i = 0; i < 8; ++i) a[i] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) a[u][i] = 0.f;
-#pragma unroll
-            for (int k = 0; k < KT; ++k) {   // destinations in ascending rank order
-                if (rrow[k] < 0) continue;
-                const uint8_t *row = p.part + (size_t)rrow[k] * p.part_stride;
-                uint4 x[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int v = v0 + 32 * u;
-                    x[u] = v < p.nvec ? ld_stream_v4(row + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    add2<OUT_F32>(a[u][0], a[u][1], x[u].x);
-                    add2<OUT_F32>(a[u][2], a[u][3], x[u].y);
-                    add2<OUT_F32>(a[u][4], a[u][5], x[u].z);
-                    add2<OUT_F32>(a[u][6], a[u][7], x[u].w);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int v = v0 + 32 * u;
-                if (v >= p.nvec) break;
-                if (OUT_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
-                                                           (size_t)v * 8);
-                    o[0] = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
-                    o[1] = make_float4(a[u][4], a[u][5], a[u][6], a[u][7]);
-                } else {
-                    uint4 o;
-                    o.x = pack_bf16x2(a[u][0], a[u][1]);
-                    o.y = pack_bf16x2(a[u][2], a[u][3]);
-                    o.z = pack_bf16x2(a[u][4], a[u][5]);
-                    o.w = pack_bf16x2(a[u][6], a[u][7]);
-                    *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
-                                               (size_t)v * 16) = o;
-                }
-            }
+        for (int k = 0; k < KT; ++k) {   // destinations in ascending rank order
+            if (!has[k]) continue;
+            add2<OUT_F32>(a[0], a[1], x[k].x);
+            add2<OUT_F32>(a[2], a[3], x[k].y);
+            add2<OUT_F32>(a[4], a[5], x[k].z);
+            add2<OUT_F32>(a[6], a[7], x[k].w);
+        }
+        if (OUT_F32) {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
+                                                   (size_t)v * 8);
+            o[0] = make_float4(a[0], a[1], a[2], a[3]);
+            o[1] = make_float4(a[4], a[5], a[6], a[7]);
+        } else {
+            uint4 o;
+            o.x = pack_bf16x2(a[0], a[1]);
+            o.y = pack_bf16x2(a[2], a[3]);
+            o.z = pack_bf16x2(a[4], a[5]);
+            o.w = pack_bf16x2(a[6], a[7]);
+            *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
+                                       (size_t)v * 16) = o;
         }
     }
 }
 
+// One-wave grid (SMs x resident CTAs) for a kernel, capped by its work.
+static int wave_grid(const void *fn, int num_sms, uint32_t items) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const long long need = ((long long)items + 255) / 256;
+    const long long wave = (long long)num_sms * per_sm;
+    return (int)(need < 1 ? 1 : (need < wave ? need : wave));
+}
+
+template <int ST>
+static cudaError_t launch_partial_st(const PartialParams &a, int num_sms, cudaStream_t st) {
+    const void *fn = (const void *)combine_partial_kernel<ST>;
+    combine_partial_kernel<ST><<<wave_grid(fn, num_sms, a.n_items), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int KT>
-static cudaError_t launch_gather_kt(const GatherParams &b, bool out_f32, int grid, cudaStream_t st) {
-    if (out_f32) combine_gather_kernel<KT, true><<<grid, 256, 0, st>>>(b);
-    else combine_gather_kernel<KT, false><<<grid, 256, 0, st>>>(b);
+static cudaError_t launch_gather_kt(const GatherParams &b, bool out_f32, int num_sms, cudaStream_t st) {
+    if (out_f32) {
+        const void *fn = (const void *)combine_gather_kernel<KT, true>;
+        combine_gather_kernel<KT, true><<<wave_grid(fn, num_sms, b.n_items), 256, 0, st>>>(b);
+    } else {
+        const void *fn = (const void *)combine_gather_kernel<KT, false>;
+        combine_gather_kernel<KT, false><<<wave_grid(fn, num_sms, b.n_items), 256, 0, st>>>(b);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine_two_stage(const PartialParams &a, const GatherParams &b, bool out_f32,
-                                     int grid, cudaStream_t st) {
-    if (a.S <= 2) combine_partial_kernel<2><<<grid, 256, 0, st>>>(a);
-    else if (a.S <= 4) combine_partial_kernel<4><<<grid, 256, 0, st>>>(a);
-    else if (a.S <= 8) combine_partial_kernel<8><<<grid, 256, 0, st>>>(a);
-    else combine_partial_kernel<16><<<grid, 256, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+                                     int num_sms, cudaStream_t st) {
+    cudaError_t e;
+    if (a.S <= 2) e = launch_partial_st<2>(a, num_sms, st);
+    else if (a.S <= 4) e = launch_partial_st<4>(a, num_sms, st);
+    else if (a.S <= 8) e = launch_partial_st<8>(a, num_sms, st);
+    else e = launch_partial_st<16>(a, num_sms, st);
     if (e != cudaSuccess) return e;
-    if (b.K <= 2) return launch_gather_kt<2>(b, out_f32, grid, st);
-    if (b.K <= 4) return launch_gather_kt<4>(b, out_f32, grid, st);
-    if (b.K <= 8) return launch_gather_kt<8>(b, out_f32, grid, st);
-    return launch_gather_kt<16>(b, out_f32, grid, st);
+    if (b.K <= 2) return launch_gather_kt<2>(b, out_f32, num_sms, st);
+    if (b.K <= 4) return launch_gather_kt<4>(b, out_f32, num_sms, st);
+    if (b.K <= 8) return launch_gather_kt<8>(b, out_f32, num_sms, st);
+    return launch_gather_kt<16>(b, out_f32, num_sms, st);
 }
 
 // Zero the rows of every expert at or past its row count, in every segment

@@ -323,7 +323,8 @@ cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool 
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);
 cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st);
 cudaError_t launch_scale_move(const ScaleMoveParams &p, int grid, cudaStream_t st);
+// both stages as one-wave grids over num_sms SMs
 cudaError_t launch_combine_two_stage(const PartialParams &a, const GatherParams &b, bool out_f32,
-                                     int grid, cudaStream_t st);
+                                     int num_sms, cudaStream_t st);
 
 }  // namespace ep
