@@ -94,6 +94,24 @@ def test_agrs_matches_oracle(dev, case):
         _compare(_host(out, f32), exp, f32)
 
 
+@pytest.mark.parametrize("W,E,K,T,h,pad", [
+    (64, 1024, 16, 6, 64, 0.1),    # the library's limits on W, E and top_k
+    (4, 8, 4, 33, 32, 0.0),        # top_k > e_local: several experts of a token on one rank
+    (1, 6, 3, 50, 64, 0.1),        # one rank: the route is the single fold
+    (3, 12, 2, 70, 8, 0.2),        # 16-byte rows, odd sizes
+])
+def test_agrs_edge_shapes(dev, W, E, K, T, h, pad):
+    s = wl.WorkloadSpec("agrs-edge", W=W, E=E, K=K, T=T, h=h, pad_frac=pad, seed=5 * W + E + T)
+    x = wl.make(s, num_tokens=np.maximum(T - np.arange(W) % 3, 0).astype(np.int32))
+    for f32 in (False, True):
+        out, buf = _run(x, dev, f32)
+        assert int(buf.status.item()) == 0
+        _check_gather(buf, x)
+        exp, err = ref.agrs(W, E, K, T, x.a1, x.topk_ids, x.topk_weights, x.num_tokens, f32)
+        assert err == 0
+        _compare(_host(out, f32), exp, f32)
+
+
 @pytest.mark.parametrize("cfg", [3, 4, 5])
 def test_agrs_full_size_sampled(dev, cfg):
     """Full-size workloads on the GPU against the oracle on sampled tokens: a

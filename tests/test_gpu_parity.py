@@ -237,12 +237,7 @@ def test_repeated_steps_are_identical(dev):
         assert torch.equal(a, outs[0][0]) and torch.equal(b.view(torch.int16), outs[0][1].view(torch.int16))
 
 
-@pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (3, 128), (4, 96), (5, 40)])
-def test_two_stage_combine_matches_page_mode_oracle(dev, cfg, T):
-    """ep_combine_two_stage restates the page's own finalize (bf16 per-rank partials,
-    summed over ranks in the output type): bit-identical to the oracle's page-mode
-    combine, and within the page's bound of the single-rounding fold."""
-    x = wl.make(wl.spec(cfg, T=T) if T else wl.spec(cfg))
+def _check_two_stage(x, dev):
     s = x.spec
     ctx = H.make_ctx(x, dev, sendbuf=True)
     a1, ids, w, nt, extras = H.inputs_dev(x, dev)
@@ -263,6 +258,24 @@ def test_two_stage_combine_matches_page_mode_oracle(dev, cfg, T):
         gf = g if f32 else wl.bf16_bits_to_f32(g)
         sf = single if f32 else wl.bf16_bits_to_f32(single)
         assert np.linalg.norm(gf.astype(np.float64) - sf) <= 1e-2 * np.linalg.norm(sf)
+
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (3, 128), (4, 96), (5, 40)])
+def test_two_stage_combine_matches_page_mode_oracle(dev, cfg, T):
+    """ep_combine_two_stage restates the page's own finalize (bf16 per-rank partials,
+    summed over ranks in the output type): bit-identical to the oracle's page-mode
+    combine, and within the page's bound of the single-rounding fold."""
+    _check_two_stage(wl.make(wl.spec(cfg, T=T) if T else wl.spec(cfg)), dev)
+
+
+@pytest.mark.parametrize("W,E,K,T,h,pad", [
+    (64, 1024, 16, 20, 64, 0.1),   # top_k 16: sixteen send rows per token to order, wide slots
+    (4, 8, 4, 33, 32, 0.0),        # top_k > e_local: two columns in every slot
+    (1, 6, 3, 50, 64, 0.1),        # one rank
+    (3, 12, 2, 300, 8, 0.2),       # two routing tiles per rank, ragged tail, 16-byte rows
+])
+def test_two_stage_combine_edge_shapes(dev, W, E, K, T, h, pad):
+    _check_two_stage(_custom(W, E, K, T, h, seed=3 * W + E + T, pad=pad), dev)
 
 
 @pytest.mark.parametrize("path", ["fused", "sendbuf"])
