@@ -80,7 +80,7 @@ void compute_layout(const ep_config_t *c, Layout *L) {
     const size_t pairs = (size_t)W * Tm * K;
     const size_t slots = (size_t)W * W * Tm * L->S;
     L->hdr = take(sizeof(ep::DevHeader));
-    L->tile_flag = take((size_t)L->num_tiles * 4);
+    L->tile_flag = take((size_t)L->num_tiles * ep::kFlagStride * 4);
     L->tile_agg = take((size_t)L->num_tiles * L->n_ctr * 4);
     L->tile_incl = take((size_t)L->num_tiles * L->n_ctr * 4);
     L->send_cnt = take((size_t)W * W * 4);

@@ -20,6 +20,10 @@ constexpr int kAlign = 256;                     // workspace sub-buffer alignmen
 constexpr int kMaxDst = EP_MAX_TOPK;            // destinations of one row, at most
 constexpr int kMaxSeg = 1 + EP_MAX_EXTRA;       // a1 + extra payloads
 constexpr uint32_t kMoveSmemBudget = 200 * 1024;  // stage memory of one mover CTA
+// Each routing tile's flag sits on its own 128-byte line: the flags are polled
+// by the look-back of later tiles and by the row movers, and on one shared
+// line those polls would queue the tiles' own release stores behind them.
+constexpr int kFlagStride = 32;                 // uint32 words between two tiles' flags
 
 // Device-side status block at the start of the workspace.
 struct DevHeader {

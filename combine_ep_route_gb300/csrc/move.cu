@@ -69,7 +69,8 @@ __device__ __forceinline__ void unit_meta(const MoveParams &p, const int32_t *pr
             // has published its outputs, then read them past the L1
             const uint32_t s = fastdiv((uint32_t)u, p.div_tm);
             const int t = u - (int)s * p.Tm;
-            const uint32_t *flag = p.tile_flag + (int)s * p.tiles_per_rank + t / kRouteTile;
+            const uint32_t *flag =
+                p.tile_flag + (size_t)((int)s * p.tiles_per_rank + t / kRouteTile) * kFlagStride;
             bool ready = true;
             if (lane == 0) ready = wait_tile_done(flag, epoch, p.wait_limit_ns, p.hdr);
             ready = __shfl_sync(0xffffffffu, ready, 0);

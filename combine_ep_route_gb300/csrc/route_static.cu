@@ -54,7 +54,7 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     const int num_tiles = W * tiles_per_rank;
     const int n_ctr = W + cfg->E;
     const size_t off_flag = align_region(sizeof(ep::DevHeader));
-    const size_t off_agg = off_flag + align_region((size_t)num_tiles * 4);
+    const size_t off_agg = off_flag + align_region((size_t)num_tiles * ep::kFlagStride * 4);
     const size_t off_incl = off_agg + align_region((size_t)num_tiles * n_ctr * 4);
     const size_t need = off_incl + align_region((size_t)num_tiles * n_ctr * 4);
     if (need > (size_t)EP_STATIC_SCRATCH_BYTES) return EP_ERR_SCRATCH_LIMIT;

@@ -192,14 +192,15 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
         for (int c = tid; c < n_ctr; c += kRouteThreads) p.tile_agg[(size_t)q * vec + c] = agg[c];
         __syncthreads();
         if (tid == 0 && publish) {
-            st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagAgg);
+            st_release_u32(&p.tile_flag[(size_t)q * kFlagStride], (epoch << 2) | kFlagAgg);
         }
         int pidx = q - 1;
         for (;;) {
             if (warp == 0) {
                 const int idx = pidx - lane;
                 uint32_t st = 0;
-                if (idx >= 0) st = wait_tile_flag(&p.tile_flag[idx], epoch, p.wait_limit_ns, p.hdr);
+                if (idx >= 0)
+                    st = wait_tile_flag(&p.tile_flag[(size_t)idx * kFlagStride], epoch, p.wait_limit_ns, p.hdr);
                 // a prefix (or a timed-out wait, whose tile is then marked bad) ends the walk
                 const uint32_t inc = __ballot_sync(0xffffffffu, idx >= 0 && st >= kFlagIncl);
                 if (__any_sync(0xffffffffu, st == kFlagTimeout) && lane == 0) s_bad = 1;
@@ -241,7 +242,7 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
     }
     for (int c = tid; c < n_ctr; c += kRouteThreads) p.tile_incl[(size_t)q * vec + c] = excl[c] + agg[c];
     __syncthreads();
-    if (tid == 0 && publish) st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagIncl);
+    if (tid == 0 && publish) st_release_u32(&p.tile_flag[(size_t)q * kFlagStride], (epoch << 2) | kFlagIncl);
 
     // 4. one thread per (token, k) pair. (a) Each pair's row, weight and send
     // slot are written (coalesced) and published: that is all the row movers of
@@ -297,7 +298,7 @@ __device__ void route_tile(const RouteParams &p, const int q, const uint32_t epo
         p.pair_send[g * K + k] = psend;
     }
     __syncthreads();
-    if (tid == 0 && publish) st_release_u32(&p.tile_flag[q], (epoch << 2) | kFlagDone);
+    if (tid == 0 && publish) st_release_u32(&p.tile_flag[(size_t)q * kFlagStride], (epoch << 2) | kFlagDone);
 
     for (int pi = tid; pi < rows_in_tile * KT; pi += kRouteThreads) {
         const int tl = pi / KT, k = pi % KT;

@@ -333,7 +333,7 @@ typedef struct ep_route_outputs {
  * routine. Its scratch is a static device array of EP_STATIC_SCRATCH_BYTES
  * (4 MiB) that every GPU loading this library holds until the process exits.
  * Problems needing more scratch than that -- roughly
- * W * ceil(max_tokens / 64) * (W + E) * 8 bytes -- are refused with
+ * W * ceil(max_tokens / 64) * ((W + E) * 8 + 128) bytes -- are refused with
  * EP_ERR_SCRATCH_LIMIT before anything is enqueued.
  *
  * The caller passes inputs (device: num_tokens or NULL, topk_ids, topk_weights,
