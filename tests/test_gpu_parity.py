@@ -224,8 +224,10 @@ def test_launch_options_do_not_change_results(dev, opts, path):
     _roundtrip(x, dev, opts=opts, path=path, ctx_kw=dict(sendbuf=path == "sendbuf"))
 
 
-def test_repeated_steps_are_identical(dev):
-    x = wl.make(wl.spec(5, T=64))
+# 32 routing tiles (every CTA routes) and 96 (32 elected routers)
+@pytest.mark.parametrize("T", [64, 160])
+def test_repeated_steps_are_identical(dev, T):
+    x = wl.make(wl.spec(5, T=T))
     ctx = H.make_ctx(x, dev)
     a1, ids, w, nt, extras = H.inputs_dev(x, dev)
     outs = []
@@ -300,11 +302,13 @@ def test_weight_on_input_top1(dev, path):
     assert np.array_equal(H.bits_host(y).reshape(-1, s.h), exp)
 
 
-def test_graph_replay_on_new_inputs(dev):
+@pytest.mark.parametrize("T", [64, 160])
+def test_graph_replay_on_new_inputs(dev, T):
     """A dispatch + combine captured once in a CUDA graph and replayed on new
     inputs copied into the same buffers stays exact: the routing look-back epoch
-    advances on the device, so no host call is needed between replays."""
-    xs = [wl.make(wl.spec(5, T=64), seed=s) for s in (11, 12, 13)]
+    and the launch's counters (tickets, routers, units) are rearmed on the device,
+    so no host call is needed between replays."""
+    xs = [wl.make(wl.spec(5, T=T), seed=s) for s in (11, 12, 13)]
     x0 = xs[0]
     s = x0.spec
     ctx = H.make_ctx(x0, dev)
