@@ -59,6 +59,17 @@ def parse():
                          "captured CUDA graph of dispatch + combine (the default)")
     ap.add_argument("--route", default="a2a", choices=["a2a", "agrs"],
                     help="agrs: time the all-gather / reduce-scatter route instead (auxiliary line)")
+    ap.add_argument("--top-k", type=int, default=None, help="override top_k of the workload")
+    ap.add_argument("--x-dtype", default="bf16", choices=["bf16", "fp8", "fp4x2"],
+                    help="dispatched rows as opaque fp8 (h bytes) or packed fp4 (h/2 bytes) with "
+                         "their scales as an extra payload (fp32 per 128 values, or one byte per "
+                         "16 values); the combine reduces a separate bf16 expert-output buffer")
+    ap.add_argument("--weight-on-input", action="store_true",
+                    help="apply_router_weight_on_input (needs --top-k 1)")
+    ap.add_argument("--ragged", action="store_true",
+                    help="tokens per rank drawn uniformly in [T/2, T] (seeded)")
+    ap.add_argument("--zero-pad", action="store_true",
+                    help="also zero every batched-expert row past the expert's count, as the page does")
     ap.add_argument("--hot", action="store_true",
                     help="no L2 flush between timed steps: the L2-resident figure of a small "
                          "workload, reported beside the flushed one, never as the headline")
@@ -81,16 +92,18 @@ def workload_counts(x: wl.Workload):
     return n_pairs, n_tok_routed, n_tok
 
 
-def algorithmic_bytes(x: wl.Workload, out_bytes_per_elem: int = 2):
+def algorithmic_bytes(x: wl.Workload, out_bytes_per_elem: int = 2, x_row_bytes: int = 0,
+                      extra_bytes: int = -1):
     """(dispatch bytes, combine bytes): each routed token row (+ extras) read
     once and written once per pair; each pair row read once and each output row
-    written once. Metadata (ids, weights, maps; < 1 %) is not counted."""
+    written once. Metadata (ids, weights, maps; < 1 %) is not counted. The
+    dispatched row may be narrower than the bf16 expert output (quantised rows)."""
     s = x.spec
     n_pairs, n_tok_routed, n_tok = workload_counts(x)
-    bx = 2 * s.h
-    bp = sum(x.extra_row_bytes)
+    bx = x_row_bytes or 2 * s.h
+    bp = sum(x.extra_row_bytes) if extra_bytes < 0 else extra_bytes
     disp = (bx + bp) * (n_tok_routed + n_pairs)
-    comb = bx * n_pairs + out_bytes_per_elem * s.h * n_tok
+    comb = 2 * s.h * n_pairs + out_bytes_per_elem * s.h * n_tok
     return disp, comb
 
 
@@ -219,10 +232,26 @@ def workload_spec(args):
         over["E"] = args.experts
     if args.hidden:
         over["h"] = args.hidden
+    if getattr(args, "top_k", None):
+        over["K"] = args.top_k
     s = wl.spec(args.config, **over)
     if over:
-        s = wl.spec(args.config, name=f"{s.name}-override-T{s.T}-E{s.E}-h{s.h}", **over)
+        s = wl.spec(args.config, name=f"{s.name}-override-T{s.T}-E{s.E}-K{s.K}-h{s.h}", **over)
     return s
+
+
+def variant_of(args) -> dict:
+    """The dispatch variant a run measures, empty for the headline path."""
+    v = {}
+    if args.x_dtype != "bf16":
+        v["x_dtype"] = args.x_dtype
+    if args.weight_on_input:
+        v["weight_on_input"] = True
+    if args.ragged:
+        v["ragged"] = "num_tokens ~ U[T/2, T] per rank, seed 7"
+    if args.zero_pad:
+        v["zero_pad"] = True
+    return v
 
 
 def dist_env():
@@ -307,17 +336,42 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    x = wl.make(workload_spec(args))
+    variant = variant_of(args)
+    spec = workload_spec(args)
+    nt_draw = None
+    if args.ragged:
+        nt_draw = np.random.default_rng(7).integers(spec.T // 2, spec.T + 1, size=spec.W).astype(np.int32)
+    x = wl.make(spec, num_tokens=nt_draw)
     s = x.spec
-    cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(x.extra_row_bytes),
-                   sendbuf=args.path == "sendbuf" or args.combine == "two_stage")
+    quant = args.x_dtype != "bf16"
+    extra_row_bytes = list(x.extra_row_bytes)
+    if quant:
+        # opaque quantised rows and their scales, sized as the pages' one-sided manager
+        # assumes: fp8 with one fp32 scale per 128 values, packed fp4 with one byte per 16
+        rng = np.random.default_rng(1000 + args.config)
+        xb = s.h if args.x_dtype == "fp8" else s.h // 2
+        sb = (s.h // 128) * 4 if args.x_dtype == "fp8" else s.h // 16
+        sb = (sb + 15) // 16 * 16
+        a1_host = rng.integers(0, 256, size=(s.W, s.T, xb), dtype=np.uint8)
+        extra_host = [rng.integers(0, 256, size=(s.W, s.T, sb), dtype=np.uint8)] + list(x.extras)
+        extra_row_bytes = [sb] + extra_row_bytes
+    cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(extra_row_bytes),
+                   sendbuf=args.path == "sendbuf" or args.combine == "two_stage",
+                   x_dtype=args.x_dtype, weight_on_input=args.weight_on_input, zero_pad=args.zero_pad)
     ctx = EpContext(cfg, dev)
-    a1 = torch.from_numpy(x.a1.view(np.int16)).to(dev).view(torch.bfloat16)
+    if quant:
+        a1 = torch.from_numpy(a1_host).to(dev).view(cfg.x_torch_dtype)
+        extras = [torch.from_numpy(e).to(dev) for e in extra_host]
+    else:
+        a1 = torch.from_numpy(x.a1.view(np.int16)).to(dev).view(torch.bfloat16)
+        extras = [torch.from_numpy(e).to(dev) for e in x.extras]
     ids = torch.from_numpy(x.topk_ids).to(dev)
     w = torch.from_numpy(x.topk_weights).to(dev)
     nt = torch.from_numpy(x.num_tokens).to(dev)
-    extras = [torch.from_numpy(e).to(dev) for e in x.extras]
     out = ctx.alloc_dispatch_outputs()
+    # identity experts read the dispatched rows; quantised rows need a bf16 expert output
+    expert_out = out.b_a1 if not quant else torch.zeros(
+        (s.W, s.E // s.W, ctx.expert_cap, s.h), dtype=torch.bfloat16, device=dev)
     y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -326,7 +380,7 @@ def run_ours(args):
 
     def step():
         ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
-        combine(out.b_a1, out=y)
+        combine(expert_out, out=y)
 
     n_warm = max(3, args.warmup)
     for _ in range(n_warm):
@@ -383,7 +437,7 @@ def run_ours(args):
     step_ms_ev, _ = timed_region()
     kt = ctx.kernel_times()
     ctx.set_option(L.EP_OPT_KERNEL_TIMING, 0)
-    disp_b, comb_b = algorithmic_bytes(x)
+    disp_b, comb_b = algorithmic_bytes(x, x_row_bytes=cfg.x_row_bytes, extra_bytes=sum(extra_row_bytes))
     n_pairs, n_tok_routed, n_tok = workload_counts(x)
     ms, _, value = replica_aggregate(sum(step_ms) / n, n_tok, dist if world > 1 else None, dev)
     peak, peak_src = measured_peaks()
@@ -404,10 +458,10 @@ def run_ours(args):
     traffic = traffic_for(dom, args.config)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not variant:
         e2e = run_e2e(ctx, x, dev, out, n, stream, combine)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not variant:
         cpu = cpu_baseline(args.config)
 
     line = {
@@ -415,12 +469,15 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": s.name, "W": s.W, "E": s.E, "top_k": s.K, "tokens_per_rank": s.T,
-                   "hidden": s.h, "extra_row_bytes": list(x.extra_row_bytes), "path": args.path,
+                   "hidden": s.h, "extra_row_bytes": list(extra_row_bytes), "path": args.path,
                    "combine": args.combine, "launch": "cuda graph replay" if args.graph else "stream",
-                   "out_dtype": "bf16", "accumulate": "f32", "experts": "identity (expert_out = b_a1)",
+                   "out_dtype": "bf16", "accumulate": "f32",
+                   "experts": ("identity (expert_out = b_a1)" if not quant else
+                               "a bf16 expert-output buffer (the dispatched rows are quantised)"),
                    "l2": ("hot: no flush between steps" if args.hot else
                           "flushed: 256 MiB write before every step, outside the step's events"),
-                   "replicas": world},
+                   "replicas": world, **({"variant": variant} if variant else {})},
+        "num_tokens": x.num_tokens.tolist() if args.ragged else None,
         "ms_per_step_median": float(np.median(step_ms)),
         "effective_gbs": (disp_b + comb_b) / (ms * 1e-3) / 1e9,
         "effective_frac_of_peak": (disp_b + comb_b) / (ms * 1e-3) / 1e9 / peak,

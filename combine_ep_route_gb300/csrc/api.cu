@@ -119,8 +119,8 @@ struct ep_ctx {
     int combine_ctas_per_sm;
     int fused_dispatch;      // routing and row movement in one persistent launch
     int route_ctas;          // CTAs of that launch that route (0 = all, -1 = chosen per problem)
-    int move_chunk_target;   // bytes; 0 = whole rows
-    int move_max_stages;
+    int move_chunk_target;   // bytes; 0 = whole rows, -1 = chosen per problem
+    int move_max_stages;     // -1 = chosen per problem (as move_pipes)
     // counters and event timing
     int64_t launches[EP_K_COUNT];
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[EP_K_COUNT];
@@ -221,30 +221,61 @@ void fill_move_common(const ep_ctx *c, ep::MoveParams &m) {
 // mover CTA for the current options.
 // Chunks per row: the largest count whose chunk is at least the target size
 // and a multiple of 16 bytes that divides the activation row.
-int move_chunks(const ep_ctx *c) {
+int move_chunks(const ep_ctx *c, int chunk_target) {
     const uint32_t a1b = (uint32_t)x_row_bytes(&c->cfg);
-    if (c->move_chunk_target == 0) return 1;
+    if (chunk_target == 0) return 1;
     int best = 1;
     for (int n = 2; n <= 64; ++n) {
         if (a1b % (16u * n) != 0) continue;
-        if (a1b / n < (uint32_t)c->move_chunk_target) break;
+        if (a1b / n < (uint32_t)chunk_target) break;
         best = n;
     }
     return best;
 }
 
-void move_shape(const ep_ctx *c, int chunks, int &pipes, int &stages, uint32_t &stage_bytes,
-                size_t &smem) {
+// The mover's unit size, pipelines per CTA and stages per pipeline: the
+// options where set, else chosen per problem. Measured on GB300 (one-launch
+// dispatch, prefill shape unless noted): small bulk copies (1 KiB, or 2 KiB
+// on four pipelines) lose up to 2x; with top_k <= 2 a unit writes little, so
+// larger units on four pipelines win (top_k 1: 57 us vs 78 us with the
+// top_k-8 shape); rows of at most 4 KiB move best whole on eight pipelines of
+// two stages (packed fp4 rows 80 vs 88 us, decode 24.1 vs 25.3 us); chunks of
+// 3 KiB or more do better on four pipelines (fp8 rows 105 vs 115 us); bf16
+// rows with top_k 8 are fastest in 2 KiB chunks, eight pipelines, four stages.
+// The slot-sourced and send-buffer steps keep that last shape.
+void move_options(const ep_ctx *c, int mode, int &chunk_target, int &pipes, int &max_stages) {
+    chunk_target = 2048;
+    pipes = 8;
+    max_stages = 4;
+    if (mode == ep::MOVE_FUSED) {
+        const long long a1b = x_row_bytes(&c->cfg);
+        if (c->cfg.top_k <= 2) {
+            chunk_target = 4096;
+            pipes = 4;
+        } else if (a1b <= 4096) {
+            chunk_target = 0;
+            max_stages = 2;
+        } else if (a1b / move_chunks(c, chunk_target) >= 3072) {
+            pipes = 4;
+        }
+    }
+    if (c->move_chunk_target >= 0) chunk_target = c->move_chunk_target;
+    if (c->move_pipes > 0) pipes = c->move_pipes;
+    if (c->move_max_stages > 0) max_stages = c->move_max_stages;
+}
+
+void move_shape(const ep_ctx *c, int chunks, int want_pipes, int max_stages, int &pipes, int &stages,
+                uint32_t &stage_bytes, size_t &smem) {
     const uint32_t a1b = (uint32_t)x_row_bytes(&c->cfg);
     stage_bytes = (uint32_t)align_up(a1b / chunks + (c->L.row_bytes - a1b), 128);
     const int ctas = c->move_ctas_per_sm;
     size_t budget = ctas == 1 ? ep::kMoveSmemBudget : (size_t)(220 * 1024) / ctas - 2048;
     if (budget > ep::kMoveSmemBudget) budget = ep::kMoveSmemBudget;
     int total = (int)(budget / stage_bytes);
-    pipes = c->move_pipes;
+    pipes = want_pipes;
     while (pipes > 1 && total / pipes < 2) --pipes;
     stages = total / pipes;
-    if (stages > c->move_max_stages) stages = c->move_max_stages;
+    if (stages > max_stages) stages = max_stages;
     if (stages < 2) stages = 2;
     const int W = c->cfg.W;
     smem = (size_t)pipes * stages * stage_bytes + (size_t)pipes * stages * 8 +
@@ -265,11 +296,13 @@ void build_move(ep_ctx *c, int mode, const void *a1, const void *const *extra_in
     // into chunks so every pipeline gets many equal units. Slot-sourced steps
     // (exchange, deliver) have one unit per sent slot, already plentiful: whole
     // rows keep the bulk copies per byte low.
-    const int chunks = (mode == ep::MOVE_FUSED || mode == ep::MOVE_PACK) ? move_chunks(c) : 1;
+    int chunk_target, want_pipes, max_stages;
+    move_options(c, mode, chunk_target, want_pipes, max_stages);
+    const int chunks = (mode == ep::MOVE_FUSED || mode == ep::MOVE_PACK) ? move_chunks(c, chunk_target) : 1;
     int pipes, stages;
     uint32_t stage_bytes;
     size_t smem;
-    move_shape(c, chunks, pipes, stages, stage_bytes, smem);
+    move_shape(c, chunks, want_pipes, max_stages, pipes, stages, stage_bytes, smem);
     m.pipes = pipes;
     m.stages = stages;
     m.stage_bytes = stage_bytes;
@@ -351,13 +384,13 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->timing = 0;
     c->pdl = 0;   // measured: the step is faster without programmatic dependent launch
     c->move_ctas_per_sm = 1;
-    c->move_pipes = 8;
+    c->move_pipes = -1;
     c->fault_skip = -1;
     c->combine_ctas_per_sm = 0;   // 0 = as many as fit (occupancy)
     c->fused_dispatch = 1;
     c->route_ctas = -1;
-    c->move_chunk_target = 2048;
-    c->move_max_stages = 4;
+    c->move_chunk_target = -1;
+    c->move_max_stages = -1;
     for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
     *out = c;
     return EP_OK;
@@ -401,7 +434,7 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
             ctx->move_ctas_per_sm = (int)value;
             return EP_OK;
         case EP_OPT_MOVE_PIPES:
-            if (value < 1 || value > 8) return EP_ERR_INVALID_ARG;
+            if (value != -1 && (value < 1 || value > 8)) return EP_ERR_INVALID_ARG;
             ctx->move_pipes = (int)value;
             return EP_OK;
         case EP_OPT_FAULT_SKIP_PUBLISH:
@@ -413,11 +446,11 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
             ctx->combine_ctas_per_sm = (int)value;
             return EP_OK;
         case EP_OPT_MOVE_CHUNK_BYTES:
-            if (value < 0 || value > (1 << 20) || value % 16 != 0) return EP_ERR_INVALID_ARG;
+            if (value != -1 && (value < 0 || value > (1 << 20) || value % 16 != 0)) return EP_ERR_INVALID_ARG;
             ctx->move_chunk_target = (int)value;
             return EP_OK;
         case EP_OPT_MOVE_MAX_STAGES:
-            if (value < 2 || value > 32) return EP_ERR_INVALID_ARG;
+            if (value != -1 && (value < 2 || value > 32)) return EP_ERR_INVALID_ARG;
             ctx->move_max_stages = (int)value;
             return EP_OK;
         case EP_OPT_FUSED_DISPATCH:

@@ -257,16 +257,19 @@ const char *ep_error_string(int code);
 #define EP_OPT_KERNEL_TIMING 2   /* 1: record CUDA events around every kernel */
 #define EP_OPT_PDL 3             /* 1: programmatic dependent launch between kernels (default 0) */
 #define EP_OPT_MOVE_CTAS_PER_SM 4 /* row-mover CTAs per SM (default 1) */
-#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA (default 8); in the
+#define EP_OPT_MOVE_PIPES 5      /* row-mover pipelines (warps) per CTA, 1..8; in the
                                     one-launch fused dispatch, the warps of its 256 that move
-                                    rows once routing is done */
+                                    rows once routing is done. -1 (default) = chosen per
+                                    problem (EP_OPT_MOVE_* together: by top_k and row size) */
 #define EP_OPT_FAULT_SKIP_PUBLISH 6 /* test hook: the routing tile with this ticket never
                                        publishes, so its successors' waits run out and
                                        report EP_ERR_TIMEOUT; -1 (default) = off */
 #define EP_OPT_COMBINE_CTAS_PER_SM 7 /* combine CTAs per SM (default 0 = all that fit) */
 #define EP_OPT_MOVE_CHUNK_BYTES 8 /* row-mover unit: rows split into chunks of at least this
-                                     many bytes (multiple of 16; 0 = whole rows; default 2048) */
-#define EP_OPT_MOVE_MAX_STAGES 9  /* row-mover stages per pipeline, at most (2..32, default 4) */
+                                     many bytes (multiple of 16; 0 = whole rows; -1 = default,
+                                     chosen per problem) */
+#define EP_OPT_MOVE_MAX_STAGES 9  /* row-mover stages per pipeline, at most (2..32; -1 = default,
+                                     chosen per problem) */
 #define EP_OPT_FUSED_DISPATCH 10  /* 1 (default): the fused path routes and moves rows in one
                                      persistent launch, movement starting as tiles finish */
 #define EP_OPT_ROUTE_CTAS 11      /* one-launch fused dispatch: how many CTAs route (the first

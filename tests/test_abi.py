@@ -172,13 +172,15 @@ def test_options(lib):
           (L.EP_OPT_COMBINE_CTAS_PER_SM, 0), (L.EP_OPT_MOVE_CHUNK_BYTES, 4096),
           (L.EP_OPT_MOVE_CHUNK_BYTES, 0), (L.EP_OPT_MOVE_MAX_STAGES, 16), (L.EP_OPT_FUSED_DISPATCH, 0),
           (L.EP_OPT_FUSED_DISPATCH, 1), (L.EP_OPT_ROUTE_CTAS, 0), (L.EP_OPT_ROUTE_CTAS, 16),
+          (L.EP_OPT_MOVE_PIPES, -1), (L.EP_OPT_MOVE_CHUNK_BYTES, -1), (L.EP_OPT_MOVE_MAX_STAGES, -1),
           (L.EP_OPT_ROUTE_CTAS, -1)]
     for o, v in ok:
         assert lib.ep_set_option(h, o, v) == 0, (o, v)
     bad = [(0, 1), (99, 1), (L.EP_OPT_WAIT_LIMIT_NS, 10), (L.EP_OPT_KERNEL_TIMING, 2),
            (L.EP_OPT_MOVE_CTAS_PER_SM, 0), (L.EP_OPT_MOVE_PIPES, 9), (L.EP_OPT_FAULT_SKIP_PUBLISH, 10**6),
            (L.EP_OPT_MOVE_CHUNK_BYTES, 100), (L.EP_OPT_MOVE_MAX_STAGES, 1), (L.EP_OPT_COMBINE_CTAS_PER_SM, 17),
-           (L.EP_OPT_ROUTE_CTAS, -2), (L.EP_OPT_ROUTE_CTAS, 4097)]
+           (L.EP_OPT_ROUTE_CTAS, -2), (L.EP_OPT_ROUTE_CTAS, 4097), (L.EP_OPT_MOVE_PIPES, -2),
+           (L.EP_OPT_MOVE_PIPES, 0), (L.EP_OPT_MOVE_CHUNK_BYTES, -16), (L.EP_OPT_MOVE_MAX_STAGES, -2)]
     for o, v in bad:
         assert lib.ep_set_option(h, o, v) == L.EP_ERR_INVALID_ARG, (o, v)
     kt = L.EpKernelTimesC()
