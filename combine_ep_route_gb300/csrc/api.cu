@@ -674,9 +674,11 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
     cp.h = cf.hidden;
     cp.n_tokens = cf.W * cf.max_tokens;
     cp.nvec = cf.hidden / 8;
-    cp.div_nvec = ep::make_fastdiv((uint32_t)cp.nvec);
     cp.n_rows = cf.E * ctx->L.Ecap;
-    const long long total = (long long)cp.n_tokens * cp.nvec;
+    const int vpt = ep::combine_vectors_per_thread(cf.top_k);
+    cp.groups = (cp.nvec + vpt - 1) / vpt;
+    cp.div_groups = ep::make_fastdiv((uint32_t)cp.groups);
+    const long long total = (long long)cp.n_tokens * cp.groups;
     long long grid = (total + 255) / 256;
     int per_sm = ctx->combine_ctas_per_sm;
     if (per_sm == 0 && ep::combine_occupancy(cf.top_k, out_dtype == EP_F32, &per_sm) != cudaSuccess)

@@ -11,10 +11,10 @@
 // (__fmul_rn / __fadd_rn, never contracted into an FMA), rounded once to the
 // output type.
 //
-// One thread produces 16 bytes of bf16 input (8 elements) of one token: it
-// reads its token's row indices and weights (shared by the threads of the
-// token through L1), issues all top_k 16-byte loads before using any, then
-// folds. Expert rows are streamed (no L1 allocation); HBM sees each pair row
+// One thread produces 16 bytes of bf16 input (8 elements) of one token -- or
+// 2 or 4 such vectors when top_k is at most 4 or 2: it reads its token's row
+// indices and weights (shared by the threads of the token through L1), issues
+// all its 16-byte loads before using any, then folds. Expert rows are streamed (no L1 allocation); HBM sees each pair row
 // read once and each output row written once.
 #include "ep_internal.cuh"
 
@@ -46,16 +46,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace
 
+// Vectors per thread: a thread keeps about eight 16-byte loads in flight
+// whatever top_k is (top_k 1: a thread reading one vector left HBM idle).
+__host__ __device__ constexpr int vectors_per_thread(int kmax) { return kmax <= 2 ? 4 : (kmax <= 4 ? 2 : 1); }
+
 template <int KMAX, bool OUT_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+    constexpr int V = vectors_per_thread(KMAX);
     pdl_wait();   // expert_out may be the previous kernel's output
-    const int nvec = p.nvec, K = p.K;
-    const uint32_t total = (uint32_t)p.n_tokens * (uint32_t)nvec;   // < 2^31
+    const int nvec = p.nvec, K = p.K, G = p.groups;
+    const uint32_t total = (uint32_t)p.n_tokens * (uint32_t)G;   // < 2^31
     const size_t row_bytes = (size_t)p.h * 2;
     for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += gridDim.x * blockDim.x) {
-        const int g = (int)fastdiv(idx, p.div_nvec);
-        const int v = (int)(idx - (uint32_t)g * (uint32_t)nvec);
+        const int g = (int)fastdiv(idx, p.div_groups);
+        const int q = (int)(idx - (uint32_t)g * (uint32_t)G);   // vectors q, q + G, ...
         int32_t r[KMAX];
         float w[KMAX];
 #pragma unroll
@@ -64,36 +69,46 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
             if (r[k] >= p.n_rows) r[k] = -1;   // routing never writes such a row
             w[k] = k < K ? __ldg(p.pair_w + (size_t)g * K + k) : 0.f;
         }
-        uint4 x[KMAX];
+        uint4 x[KMAX][V];
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-            if (r[k] >= 0) x[k] = ld_stream_v4(p.expert_out + (size_t)r[k] * row_bytes + (size_t)v * 16);
-            else x[k] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        float a[8];
+        for (int k = 0; k < KMAX; ++k)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = 0.f;
+            for (int j = 0; j < V; ++j) {
+                const int v = q + j * G;
+                if (r[k] >= 0 && v < nvec)
+                    x[k][j] = ld_stream_v4(p.expert_out + (size_t)r[k] * row_bytes + (size_t)v * 16);
+                else
+                    x[k][j] = make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-            if (r[k] < 0) continue;
-            fold2(a[0], a[1], w[k], x[k].x);
-            fold2(a[2], a[3], w[k], x[k].y);
-            fold2(a[4], a[5], w[k], x[k].z);
-            fold2(a[6], a[7], w[k], x[k].w);
-        }
-        if (OUT_F32) {
-            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
-                                                   (size_t)v * 8);
-            o[0] = make_float4(a[0], a[1], a[2], a[3]);
-            o[1] = make_float4(a[4], a[5], a[6], a[7]);
-        } else {
-            uint4 o;
-            o.x = pack_bf16x2(a[0], a[1]);
-            o.y = pack_bf16x2(a[2], a[3]);
-            o.z = pack_bf16x2(a[4], a[5]);
-            o.w = pack_bf16x2(a[6], a[7]);
-            *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
-                                       (size_t)v * 16) = o;
+        for (int j = 0; j < V; ++j) {
+            const int v = q + j * G;
+            if (v >= nvec) break;
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k) {
+                if (r[k] < 0) continue;
+                fold2(a[0], a[1], w[k], x[k][j].x);
+                fold2(a[2], a[3], w[k], x[k][j].y);
+                fold2(a[4], a[5], w[k], x[k][j].z);
+                fold2(a[6], a[7], w[k], x[k][j].w);
+            }
+            if (OUT_F32) {
+                float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
+                                                       (size_t)v * 8);
+                o[0] = make_float4(a[0], a[1], a[2], a[3]);
+                o[1] = make_float4(a[4], a[5], a[6], a[7]);
+            } else {
+                uint4 o;
+                o.x = pack_bf16x2(a[0], a[1]);
+                o.y = pack_bf16x2(a[2], a[3]);
+                o.z = pack_bf16x2(a[4], a[5]);
+                o.w = pack_bf16x2(a[6], a[7]);
+                *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
+                                           (size_t)v * 16) = o;
+            }
         }
     }
 }
@@ -108,6 +123,10 @@ static const void *combine_fn(int K, bool out_f32) {
     if (K <= 4) return pick_combine<4>(out_f32);
     if (K <= 8) return pick_combine<8>(out_f32);
     return pick_combine<16>(out_f32);
+}
+
+int combine_vectors_per_thread(int top_k) {
+    return vectors_per_thread(top_k <= 2 ? 2 : (top_k <= 4 ? 4 : (top_k <= 8 ? 8 : 16)));
 }
 
 // Resident CTAs per SM of the combine kernel for this top_k (one full wave of

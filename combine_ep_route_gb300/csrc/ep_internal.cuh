@@ -125,7 +125,8 @@ struct CombineParams {
     int K, h, n_tokens;
     int n_rows;                  // E*Ecap: pair rows at or past it are never read
     int nvec;                    // h / 8; n_tokens * nvec < 2^31
-    FastDiv div_nvec;
+    int groups;                  // threads per token: ceil(nvec / vectors per thread)
+    FastDiv div_groups;
 };
 
 // Two-stage combine, stage 1: per received slot, the bf16-rounded fp32 sum of its
@@ -325,6 +326,9 @@ cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, i
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st);
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);
+// 16-byte vectors of one token a combine thread reduces (more for small top_k,
+// so that every thread keeps several loads in flight)
+int combine_vectors_per_thread(int top_k);
 cudaError_t launch_zero_pad(const ZeroPadParams &p, int grid_x, cudaStream_t st);
 cudaError_t launch_scale_move(const ScaleMoveParams &p, int grid, cudaStream_t st);
 // both stages as one-wave grids over num_sms SMs
