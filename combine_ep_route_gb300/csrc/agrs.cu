@@ -25,6 +25,7 @@
 #include "ep_internal.cuh"
 
 #include <cuda_bf16.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 
@@ -332,6 +333,10 @@ extern "C" int ep_agrs(const ep_config_t *cfg, const int32_t *num_tokens, const 
     p.div_Tm = make_fastdiv((uint32_t)Tm);
     p.div_ntok = make_fastdiv(p.n_tok);
 
+    struct Range {   // NVTX range over the three launches
+        Range() { nvtxRangePushA("ep:agrs"); }
+        ~Range() { nvtxRangePop(); }
+    } range;
     if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), st) != cudaSuccess) return EP_ERR_CUDA;
     agrs_gather_kernel<<<grid_for(W * Tm * (nvec + K), kThreads, wv.gather), kThreads, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return EP_ERR_CUDA;

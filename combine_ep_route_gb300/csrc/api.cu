@@ -4,6 +4,8 @@
 // per-kernel event timing used by the benchmark.
 #include "ep_internal.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstddef>
 #include <cstdlib>
 #include <cstring>
@@ -146,12 +148,20 @@ cudaEvent_t take_event(ep_ctx *c) {
 }
 
 // Records an event pair around one kernel launch when timing is on.
+const char *const kKindRange[EP_K_COUNT] = {
+    "ep:route", "ep:move_fused", "ep:pack", "ep:exchange", "ep:deliver",
+    "ep:combine", "ep:zero_pad", "ep:combine_two_stage", "ep:dispatch_fused"};
+
+// Around every library launch: a launch count, an NVTX range named for the
+// kernel (visible to Nsight tools; free when none is attached) and, with
+// EP_OPT_KERNEL_TIMING, CUDA events on the launching stream.
 struct KernelTimer {
     ep_ctx *c;
     int kind;
     cudaStream_t st;
     cudaEvent_t a = nullptr, b = nullptr;
     KernelTimer(ep_ctx *c_, int kind_, cudaStream_t st_) : c(c_), kind(kind_), st(st_) {
+        nvtxRangePushA(kKindRange[kind]);
         c->launches[kind]++;
         if (c->timing) {
             a = take_event(c);
@@ -167,6 +177,7 @@ struct KernelTimer {
             if (a) c->pool.push_back(a);
             if (b) c->pool.push_back(b);
         }
+        nvtxRangePop();
     }
 };
 

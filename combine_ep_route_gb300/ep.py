@@ -94,14 +94,24 @@ class DispatchOut:
 
 
 class EpContext:
-    """A dispatch/combine context over a workspace allocated through PyTorch."""
+    """A dispatch/combine context over a workspace allocated through PyTorch, or
+    over ``workspace`` (a contiguous uint8 device tensor of at least
+    ``workspace_bytes(cfg)`` bytes, 256-byte aligned) that the caller owns."""
 
-    def __init__(self, cfg: EpConfig, device: Optional[torch.device] = None):
+    def __init__(self, cfg: EpConfig, device: Optional[torch.device] = None,
+                 workspace: Optional[torch.Tensor] = None):
         self.cfg = cfg
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.tok_cap, self.slots, self.expert_cap = capacities(cfg)
         nbytes = workspace_bytes(cfg)
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        if workspace is None:
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        else:
+            if (workspace.dtype != torch.uint8 or not workspace.is_contiguous() or workspace.numel() < nbytes
+                    or workspace.device != self.device):
+                raise ValueError(f"workspace: want a contiguous uint8 tensor of at least {nbytes} bytes "
+                                 f"on {self.device}")
+            self.workspace = workspace[:nbytes]
         h = C.c_void_p()
         L.check(L.lib().ep_ctx_create(C.byref(cfg.to_c()), C.c_void_p(self.workspace.data_ptr()),
                                       nbytes, C.byref(h)), "ep_ctx_create")
