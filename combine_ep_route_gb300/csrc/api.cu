@@ -750,7 +750,6 @@ int ep_combine_two_stage(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtyp
     b.n_items = (uint32_t)(cf.W * cf.max_tokens) * (uint32_t)b.nvec;
     b.div_nvec = a.div_nvec;
     b.div_tm = a.div_tm;
-    b.div_w = a.div_w;
     {
         KernelTimer tm(ctx, EP_K_COMBINE_TWO_STAGE, st);
         if (ep::launch_combine_two_stage(a, b, out_dtype == EP_F32, ctx->num_sms, st) != cudaSuccess)

@@ -151,7 +151,7 @@ struct GatherParams {
     void *out;
     int W, Tm, K, h, nvec;
     uint32_t n_items;               // W*Tm*nvec
-    FastDiv div_nvec, div_tm, div_w;
+    FastDiv div_nvec, div_tm;
 };
 
 // Dispatch with apply_router_weight_on_input (top_k == 1): scaled row copies.
