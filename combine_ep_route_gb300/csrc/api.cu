@@ -119,6 +119,7 @@ struct ep_ctx {
     int move_pipes;
     int fault_skip;
     int combine_ctas_per_sm;
+    int combine_wave[2];     // resident combine CTAs per SM (bf16, f32 out), 0 until queried
     int fused_dispatch;      // routing and row movement in one persistent launch
     int route_ctas;          // CTAs of that launch that route (0 = all, -1 = chosen per problem)
     int move_chunk_target;   // bytes; 0 = whole rows, -1 = chosen per problem
@@ -398,6 +399,7 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->move_pipes = -1;
     c->fault_skip = -1;
     c->combine_ctas_per_sm = 0;   // 0 = as many as fit (occupancy)
+    c->combine_wave[0] = c->combine_wave[1] = 0;
     c->fused_dispatch = 1;
     c->route_ctas = -1;
     c->move_chunk_target = -1;
@@ -692,8 +694,12 @@ int ep_combine(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtype, void *o
     const long long total = (long long)cp.n_tokens * cp.groups;
     long long grid = (total + 255) / 256;
     int per_sm = ctx->combine_ctas_per_sm;
-    if (per_sm == 0 && ep::combine_occupancy(cf.top_k, out_dtype == EP_F32, &per_sm) != cudaSuccess)
-        return EP_ERR_CUDA;
+    if (per_sm == 0) {
+        int &cached = ctx->combine_wave[out_dtype == EP_F32 ? 1 : 0];
+        if (cached == 0 && ep::combine_occupancy(cf.top_k, out_dtype == EP_F32, &cached) != cudaSuccess)
+            return EP_ERR_CUDA;
+        per_sm = cached;
+    }
     const long long cap = (long long)ctx->num_sms * per_sm;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;

@@ -108,6 +108,8 @@ def _custom(W, E, K, T, h, seed=0, pad=0.0, extras=(), num_tokens=None):
     (2, 4, 2, 1, 16, 0.0, ()),             # one token per rank
     (64, 1024, 16, 20, 64, 0.1, (4, 12)),  # the library's limits on W, E, top_k; two extras
     (8, 64, 8, 700, 2048, 0.05, ()),       # 3 tiles per rank
+    (4, 32, 6, 150, 5120, 0.05, (16,)),    # 10 KiB rows in five 2 KiB units, top_k 6
+    (8, 64, 8, 90, 1536, 0.0, ()),         # 3 KiB rows, moved whole
 ])
 def test_edge_shapes(dev, W, E, K, T, h, pad, extras):
     _roundtrip(_custom(W, E, K, T, h, seed=W + E + T, pad=pad, extras=extras), dev, out_f32=(False, True))
