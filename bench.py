@@ -437,6 +437,22 @@ def run_ours(args):
     step_ms_ev, _ = timed_region()
     kt = ctx.kernel_times()
     ctx.set_option(L.EP_OPT_KERNEL_TIMING, 0)
+    # 3. medians of dispatch and combine timed separately (events around each call,
+    #    L2 flushed before every step), over a fixed 200 repetitions
+    reps = 200
+    evm = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        if not args.hot:
+            flush.zero_()
+        evm[i][0].record(stream)
+        ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
+        evm[i][1].record(stream)
+        combine(expert_out, out=y)
+        evm[i][2].record(stream)
+    torch.cuda.synchronize()
+    med_d = float(np.median([e[0].elapsed_time(e[1]) for e in evm]))
+    med_c = float(np.median([e[1].elapsed_time(e[2]) for e in evm]))
     disp_b, comb_b = algorithmic_bytes(x, x_row_bytes=cfg.x_row_bytes, extra_bytes=sum(extra_row_bytes))
     n_pairs, n_tok_routed, n_tok = workload_counts(x)
     ms, _, value = replica_aggregate(sum(step_ms) / n, n_tok, dist if world > 1 else None, dev)
@@ -485,6 +501,9 @@ def run_ours(args):
         "counts": {"pairs": n_pairs, "tokens_routed": n_tok_routed, "tokens": n_tok},
         "pairs_per_s": world * n_pairs / (ms * 1e-3),
         "kernel_ms": {k: round(v, 5) for k, v in per.items()},
+        "call_ms_median": {"dispatch": round(med_d, 5), "combine": round(med_c, 5),
+                           "sum": round(med_d + med_c, 5),
+                           "note": "200 eager steps, events around each call, L2 flushed per step"},
         "kernel_ms_note": "second pass of K steps with CUDA events around every launch "
                           f"(step {sum(step_ms_ev) / n:.4f} ms with those events)",
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
