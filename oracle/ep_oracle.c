@@ -13,7 +13,10 @@
  * methods it restates. It is written as slow, obvious loops: no blocking, no
  * reordering beyond what the method states. The all_to_all_single exchange of
  * the page is a plain block transpose here, because all ranks share one
- * address space: recv[d][s] = send[s][d].
+ * address space: recv[d][s] = send[s][d]. `oracle_scale_input` restates the
+ * same method's apply_router_weight_on_input branch. `oracle_agrs` follows
+ * vLLM's AgRsAll2AllManager (page device_communicators/all2all, `dispatch`
+ * and `combine`: all_gatherv, then reduce_scatterv) with identity experts.
  *
  * Readings of points the page leaves open (each also listed in the design
  * notes of the repository):
@@ -29,7 +32,11 @@
  *     one sum per step, rounded once to the output type. The page sums
  *     per-destination partials in fp32, rounds them to the activation type
  *     and sums those in the output type; `oracle_combine_pagemode` restates
- *     that two-stage form so tests can show both agree within tolerance.
+ *     that two-stage form so tests can show both agree within tolerance;
+ *   - in the AgRs route each rank applies only its own experts (the expert
+ *     map of the fused-MoE layer), rounds its output to bf16, and the
+ *     reduce-scatter sums the ranks' outputs in ascending rank order (each
+ *     sum rounded for bf16 output, fp32 sums for fp32 output).
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no FMA contraction, so each
  * product and each sum rounds on its own, as the fold above states).
