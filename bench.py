@@ -274,10 +274,10 @@ def oracle_step(x: wl.Workload):
 
 def cpu_baseline(cfg: int, budget_s: float = 12.0):
     """The oracle as it stands (one host thread) on the full workload, repeated
-    until about budget_s of CPU work."""
+    until about budget_s of CPU work (at most 64 steps)."""
     x = wl.make(cfg)
     toks, t_all, reps = 0, 0.0, 0
-    while t_all < budget_s and reps < 3:
+    while t_all < budget_s and reps < 64:
         t0 = time.perf_counter()
         toks += oracle_step(x)
         t_all += time.perf_counter() - t0
