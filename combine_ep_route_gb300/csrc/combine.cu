@@ -188,21 +188,19 @@ __global__ void __launch_bounds__(256) combine_partial_kernel(const PartialParam
                 my_w = __ldg(p.recv_w + base + lane);
             }
         }
-        // the valid columns, compacted in column order (the fold order)
+        // the valid columns, compacted in column order (the fold order); a
+        // column's row and weight stay in the lane that read them and are
+        // fetched by shuffle where they are used, which keeps registers free
+        // for more warps in flight
         const uint32_t vmask = __ballot_sync(0xffffffffu, my_src >= 0);
         const int nv = __popc(vmask);
-        int64_t src[ST];
-        float w[ST];
-#pragma unroll
-        for (int c = 0; c < ST; ++c) {
-            const int from = c < nv ? __fns(vmask, 0, c + 1) : 0;
-            src[c] = __shfl_sync(0xffffffffu, my_src, from);
-            w[c] = __shfl_sync(0xffffffffu, my_w, from);
-        }
         uint8_t *dst = p.part + (size_t)r * p.part_stride;
         // four vectors per lane per round; two columns' loads go out together, so
-        // a slot with several columns keeps twice the bytes in flight
-        for (int v0 = lane; v0 < p.nvec; v0 += 128) {
+        // a slot with several columns keeps twice the bytes in flight. The rounds
+        // are counted per warp, not per lane, so that every lane takes part in
+        // every shuffle below even when a row is shorter than the warp's span.
+        for (int vb = 0; vb < p.nvec; vb += 128) {
+            const int v0 = vb + lane;
             float a[4][8];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -212,8 +210,14 @@ __global__ void __launch_bounds__(256) combine_partial_kernel(const PartialParam
             for (int c = 0; c < ST; c += 2) {
                 if (c >= nv) break;
                 const bool two = c + 1 < nv;
-                const uint8_t *row0 = p.expert_out + (size_t)src[c] * row_bytes;
-                const uint8_t *row1 = p.expert_out + (size_t)(two ? src[c + 1] : src[c]) * row_bytes;
+                const int from0 = __fns(vmask, 0, c + 1);
+                const int from1 = two ? __fns(vmask, 0, c + 2) : from0;
+                const int64_t src0 = __shfl_sync(0xffffffffu, my_src, from0);
+                const int64_t src1 = __shfl_sync(0xffffffffu, my_src, from1);
+                const float w0 = __shfl_sync(0xffffffffu, my_w, from0);
+                const float w1 = __shfl_sync(0xffffffffu, my_w, from1);
+                const uint8_t *row0 = p.expert_out + (size_t)src0 * row_bytes;
+                const uint8_t *row1 = p.expert_out + (size_t)src1 * row_bytes;
                 uint4 x[2][4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(256) combine_partial_kernel(const PartialParam
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     if (q == 1 && !two) break;
-                    const float wc = w[c + q];
+                    const float wc = q == 0 ? w0 : w1;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         fold2(a[u][0], a[u][1], wc, x[q][u].x);
