@@ -214,3 +214,28 @@ def test_agrs_graph_replay_on_new_inputs(dev):
     torch.cuda.synchronize(dev)
     exp, _ = ref.agrs(s.W, s.E, s.K, s.T, x1.a1, x1.topk_ids, x1.topk_weights, x1.num_tokens, False)
     _compare(_host(out, False), exp, False)
+
+
+def test_agrs_worked_example_by_hand(dev):
+    """The hand-derived example of tests/golden/agrs_worked_example.json on the
+    GPU (its row padded with zeros to the kernels' 8-element granularity): the
+    rank-ordered bf16 sums round twice on ties to even and give 1.125 where the
+    single fp32 fold gives 1.1328125."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "agrs_worked_example.json")))
+    W, E, K, Tm, h = g["W"], g["E"], g["top_k"], g["max_tokens"], 8
+    a1 = np.zeros((W, Tm, h), np.float32)
+    a1[0, 0, :2] = g["a1"]
+    ids = np.full((W, Tm, K), -1, np.int32)
+    w = np.zeros((W, Tm, K), np.float32)
+    ids[0, 0] = g["topk_ids"][0]
+    w[0, 0] = g["topk_weights"][0]
+    x = wl.Workload(wl.WorkloadSpec("by-hand", W=W, E=E, K=K, T=Tm, h=h), wl.f32_to_bf16_bits(a1), ids, w,
+                    np.array(g["num_tokens"], np.int32))
+    for f32, key in ((False, "expect_bf16_out"), (True, "expect_f32_out")):
+        out, buf = _run(x, dev, f32)
+        assert int(buf.status.item()) == 0
+        got = _host(out, f32).reshape(W, h)
+        assert np.array_equal(got[:, :2], np.array(g[key], np.float32))
+        assert (got[:, 2:] == 0).all()

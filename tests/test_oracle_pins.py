@@ -449,3 +449,32 @@ def test_agrs_drops_bad_pairs_like_the_router():
     # token (0,0): only id 0 kept -> 0.25 x; token (0,1): ids 1 and 2 kept (on ranks 0 and 1)
     assert np.array_equal(out[0], wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(0.25 * x[0])))
     assert (out[2] == 0).all()
+
+
+def test_agrs_worked_example_by_hand():
+    """tests/golden/agrs_worked_example.json: a token whose three experts live on
+    three ranks. The per-rank bf16 outputs summed in rank order round twice on
+    ties (to even) and land one bf16 step below the single fp32 fold."""
+    g = json.load(open(os.path.join(os.path.dirname(GOLDEN), "agrs_worked_example.json")))
+    W, E, K, Tm, h = g["W"], g["E"], g["top_k"], g["max_tokens"], g["hidden"]
+    a1 = np.zeros((W, Tm, h), np.float32)
+    a1[0, 0] = g["a1"]
+    ids = np.full((W, Tm, K), -1, np.int32)
+    w = np.zeros((W, Tm, K), np.float32)
+    for r in range(W):
+        if g["topk_ids"][r]:
+            ids[r, 0] = g["topk_ids"][r]
+            w[r, 0] = g["topk_weights"][r]
+    nt = np.array(g["num_tokens"], np.int32)
+    x = wl.f32_to_bf16_bits(a1)
+    out, err = ref.agrs(W, E, K, Tm, x, ids, w, nt, out_f32=False)
+    assert err == 0
+    assert np.array_equal(wl.bf16_bits_to_f32(out).reshape(W, h), np.array(g["expect_bf16_out"], np.float32))
+    out32, _ = ref.agrs(W, E, K, Tm, x, ids, w, nt, out_f32=True)
+    assert np.array_equal(out32.reshape(W, h), np.array(g["expect_f32_out"], np.float32))
+    # the all-to-all route: single fold, and the page's two-stage rounding (= this route)
+    m = ref.dispatch_meta(W, E, K, Tm, ids, w, nt)
+    rows = ref.dispatch_rows(m, x)
+    single = wl.bf16_bits_to_f32(ref.combine(m, w, rows)).reshape(W, h)
+    assert np.array_equal(single[0], np.array(g["expect_single_fold_bf16"], np.float32))
+    assert np.array_equal(ref.combine_pagemode(m, rows), out)
