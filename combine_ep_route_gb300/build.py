@@ -2,7 +2,7 @@
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel with nvcc, then
 linked into ``combine_ep_route_gb300/libep.so`` (CUDA runtime linked
-statically, so the library needs only the driver at run time).
+statically, so the library needs only the NVIDIA GPU driver at run time).
 """
 from __future__ import annotations
 
