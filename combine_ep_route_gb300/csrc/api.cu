@@ -325,6 +325,25 @@ void build_move(ep_ctx *c, int mode, const void *a1, const void *const *extra_in
     smem_out = smem;
 }
 
+// Routers of the one-launch dispatch, when not set. Measured on GB300: with
+// many tiles, 32 routers working through them in ticket order keep ahead of
+// the movers while the other CTAs move rows from the outset (prefill: 174 us
+// vs 179 us with every CTA routing first); with few tiles every CTA routes.
+// The routers must publish tiles at least twice as fast as the movers consume
+// them: a tile takes a router about 4 us + 0.75 us per top_k slot under load
+// (10 us at top_k 8, from per-tile timestamps), and the movers drain a tile's
+// rows (64 tokens, one read and top_k writes) at about 6.5 TB/s. Tiles of small
+// rows therefore need more routers, up to every CTA (measured: packed fp4 rows
+// 71 vs 80 us, 512-byte rows on 256 tiles 76 vs 112 us, against 32 routers).
+int auto_route_ctas(const ep_ctx *c) {
+    if (c->L.num_tiles <= 32) return 0;
+    const double tile_bytes = (double)ep::kRouteTile * (1 + c->cfg.top_k) * (double)c->L.row_bytes;
+    const double tile_time = (4.0 + 0.75 * c->cfg.top_k) * 1e-6;
+    const double need = 2.0 * tile_time * 6.5e12 / tile_bytes;
+    if (need >= (double)c->num_sms) return 0;
+    return need > 32.0 ? (int)need + 1 : 32;
+}
+
 int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *const *extra_in,
                      void *b_a1, void *const *extra_out, bool pdl, cudaStream_t st) {
     ep::MoveParams m;
@@ -575,11 +594,7 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         fm.tile_flag = rp.tile_flag;
         fm.tiles_per_rank = L.tiles_per_rank;
         fm.div_tm = ep::make_fastdiv((uint32_t)cf.max_tokens);
-        // measured on GB300: with many tiles, 32 routers working through them in
-        // ticket order keep ahead of the movers while the other CTAs move rows
-        // from the outset (prefill: 174 us vs 179 us with every CTA routing
-        // first); with few tiles every CTA routes
-        rp.route_ctas = ctx->route_ctas >= 0 ? ctx->route_ctas : (L.num_tiles > 32 ? 32 : 0);
+        rp.route_ctas = ctx->route_ctas >= 0 ? ctx->route_ctas : auto_route_ctas(ctx);
         KernelTimer tm(ctx, EP_K_DISPATCH_FUSED, st);
         if (ep::launch_dispatch_fused(rp, fm, ctx->num_sms, fsmem, st) != cudaSuccess) return EP_ERR_CUDA;
     } else {

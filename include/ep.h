@@ -274,8 +274,9 @@ const char *ep_error_string(int code);
                                      persistent launch, movement starting as tiles finish */
 #define EP_OPT_ROUTE_CTAS 11      /* one-launch fused dispatch: how many CTAs route (the first
                                      to start; the others move rows from the outset);
-                                     0 = every CTA routes first; -1 (default) = 32 when the
-                                     problem has more than 32 routing tiles, else 0 (-1..4096) */
+                                     0 = every CTA routes first; -1 (default) = chosen per
+                                     problem: 0 up to 32 routing tiles, else enough routers to
+                                     stay ahead of the row movers, at least 32 (-1..4096) */
 
 /* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
 int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
