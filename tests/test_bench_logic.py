@@ -1,0 +1,72 @@
+"""The benchmark's measurement arithmetic, checked on the CPU against counts
+taken independently from the oracle's routing: the algorithmic bytes that the
+roofline divides by, the all-gather / reduce-scatter byte count, the DRAM
+traffic lookup and the variant bookkeeping."""
+import argparse
+
+import numpy as np
+import pytest
+
+import bench
+from combine_ep_route_gb300 import workloads as wl
+from oracle import ref
+
+
+@pytest.mark.parametrize("cfg,over", [(1, {}), (2, {}), (3, {"T": 96}), (4, {"T": 40}), (5, {"T": 20})])
+def test_algorithmic_bytes_from_the_oracles_routing(cfg, over):
+    s = wl.spec(cfg, **over)
+    x = wl.make(s, num_tokens=np.maximum(s.T - np.arange(s.W) % 5, 0).astype(np.int32))
+    m = ref.dispatch_meta(s.W, s.E, s.K, s.T, x.topk_ids, x.topk_weights, x.num_tokens)
+    # pairs = delivered rows; routed tokens = tokens holding at least one slot
+    n_pairs = int(m.expert_num_tokens.sum())
+    n_routed = len({(si, int(t)) for si in range(s.W) for d in range(s.W)
+                    for t in m.send_tok[si, d][:m.send_cnt[si, d]]})
+    bx, bp = 2 * s.h, sum(x.extra_row_bytes)
+    disp, comb = bench.algorithmic_bytes(x)
+    assert disp == (bx + bp) * (n_routed + n_pairs)
+    assert comb == bx * n_pairs + 2 * s.h * int(x.num_tokens.sum())
+    # fp32 output and a narrower dispatched row (quantised payloads)
+    _, comb32 = bench.algorithmic_bytes(x, out_bytes_per_elem=4)
+    assert comb32 == bx * n_pairs + 4 * s.h * int(x.num_tokens.sum())
+    d8, _ = bench.algorithmic_bytes(x, x_row_bytes=s.h, extra_bytes=64)
+    assert d8 == (s.h + 64) * (n_routed + n_pairs)
+
+
+def test_agrs_bytes_by_brute_force():
+    s = wl.spec(2, T=48)
+    x = wl.make(s, num_tokens=np.array([48, 10, 0, 48, 7, 30, 48, 1], np.int32))
+    parts, n_local = bench.agrs_bytes(x)
+    e_local = s.E // s.W
+    want_local, n_tok = 0, 0
+    for r in range(s.W):
+        for t in range(int(x.num_tokens[r])):
+            n_tok += 1
+            ranks = {int(e) // e_local for e in x.topk_ids[r, t] if e >= 0}
+            want_local += len(ranks)
+    assert n_local == want_local
+    row, meta = 2 * s.h, 8 * s.K
+    assert parts["gather"] == (row + meta) * n_tok * (1 + s.W)
+    assert parts["experts"] == s.W * n_tok * meta + want_local * row + s.W * n_tok * row
+    assert parts["reduce_scatter"] == s.W * n_tok * row + s.W * s.T * row
+
+
+def test_traffic_lookup_follows_the_kernel_sources(tmp_path, monkeypatch):
+    src = bench.kernel_source_hash("dispatch_fused")
+    f = tmp_path / "traffic.txt"
+    f.write_text("# comment\n"
+                 f"kernel=dispatch_fused config=3 source={src} bytes_per_launch=123\n"
+                 "kernel=combine config=3 source=0000000000000000 bytes_per_launch=456\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_for("dispatch_fused", 3) == 123.0
+    assert bench.traffic_for("dispatch_fused", 2) is None      # another workload
+    assert bench.traffic_for("combine", 3) is None             # taken on other sources
+    # a kernel's hash covers its own translation unit, not another kernel's
+    assert bench.kernel_source_hash("dispatch_fused") != bench.kernel_source_hash("combine")
+    assert bench.kernel_source_hash("agrs_gather") == bench.kernel_source_hash("agrs_reduce")
+
+
+def test_variant_bookkeeping():
+    base = argparse.Namespace(x_dtype="bf16", weight_on_input=False, ragged=False, zero_pad=False)
+    assert bench.variant_of(base) == {}
+    v = bench.variant_of(argparse.Namespace(x_dtype="fp8", weight_on_input=True, ragged=True, zero_pad=True))
+    assert v["x_dtype"] == "fp8" and v["weight_on_input"] and v["zero_pad"] and "ragged" in v
