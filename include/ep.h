@@ -10,10 +10,12 @@
  * multi-payload dispatch follow FlashInfer "MoE All-to-All Operations
  * (Throughput Backend)" (page flashinfer/comm/trtllm_moe_alltoall.py:
  * `moe_a2a_get_workspace_size_per_rank`, `MoeAlltoAll.dispatch/combine`,
- * `_A2AState`).
+ * `_A2AState`). The all-gather / reduce-scatter route (ep_agrs) follows vLLM's
+ * AgRsAll2AllManager (page device_communicators/all2all).
  *
  * Conventions for every entry point:
- *   - Return value: EP_OK (0) or a negative EP_ERR_* code; nothing else.
+ *   - Return value: EP_OK (0) or a negative EP_ERR_* code; nothing else
+ *     (ep_error_string, which returns a message, is the one exception).
  *   - "device" pointers are CUDA global-memory addresses of the current device;
  *     "host" pointers are ordinary process memory. The library never allocates
  *     device memory: the caller owns every buffer, including the workspace,
