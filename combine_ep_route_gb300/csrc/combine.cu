@@ -272,6 +272,17 @@ __device__ __forceinline__ void add2(float &a0, float &a1, uint32_t x) {
     }
 }
 
+// Two bf16 sums at once, each rounded to nearest even. For bf16 operands this
+// gives the same bits as an fp32 sum rounded to bf16: the fp32 sum is exact
+// whenever the exponents differ by at most 15, and otherwise the smaller
+// operand lies far below half a bf16 unit of the larger, so both roundings
+// return the larger.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ void cmp_swap(int &a, int &b) {
     const int lo = min(a, b), hi = max(a, b);
     a = lo;
@@ -331,28 +342,34 @@ __global__ void __launch_bounds__(256) combine_gather_kernel(const GatherParams 
                 }
             }
         }
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = 0.f;
-#pragma unroll
-        for (int k = 0; k < KT; ++k) {   // destinations in ascending rank order
-            if (!has[k]) continue;
-            add2<OUT_F32>(a[0], a[1], x[k].x);
-            add2<OUT_F32>(a[2], a[3], x[k].y);
-            add2<OUT_F32>(a[4], a[5], x[k].z);
-            add2<OUT_F32>(a[6], a[7], x[k].w);
-        }
         if (OUT_F32) {
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KT; ++k) {   // destinations in ascending rank order
+                if (!has[k]) continue;
+                add2<true>(a[0], a[1], x[k].x);
+                add2<true>(a[2], a[3], x[k].y);
+                add2<true>(a[4], a[5], x[k].z);
+                add2<true>(a[6], a[7], x[k].w);
+            }
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
                                                    (size_t)v * 8);
             o[0] = make_float4(a[0], a[1], a[2], a[3]);
             o[1] = make_float4(a[4], a[5], a[6], a[7]);
         } else {
-            uint4 o;
-            o.x = pack_bf16x2(a[0], a[1]);
-            o.y = pack_bf16x2(a[2], a[3]);
-            o.z = pack_bf16x2(a[4], a[5]);
-            o.w = pack_bf16x2(a[6], a[7]);
+            // bf16 sums, each rounded, in ascending rank order: native bf16 adds
+            // (see add_bf16x2), starting from +0 like the fp32 form
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int k = 0; k < KT; ++k) {
+                if (!has[k]) continue;
+                o.x = add_bf16x2(o.x, x[k].x);
+                o.y = add_bf16x2(o.y, x[k].y);
+                o.z = add_bf16x2(o.z, x[k].z);
+                o.w = add_bf16x2(o.w, x[k].w);
+            }
             *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
                                        (size_t)v * 16) = o;
         }
