@@ -135,10 +135,19 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, cfg: int):
+def traffic_config(args, s, variant=None):
+    """The workload key of the committed DRAM figures: the named workload's
+    number when this run measures that workload unchanged, else None (an
+    override or a variant moves other bytes than the captured ones)."""
+    if variant or s.name != wl.spec(args.config).name:
+        return None
+    return args.config
+
+
+def traffic_for(kernel: str, cfg):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
+    on the current kernel sources and the same workload (else None)."""
+    if cfg is None or not os.path.exists(TRAFFIC_FILE):
         return None
     src = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
@@ -471,7 +480,7 @@ def run_ours(args):
     # two-stage combine are charged the same algorithmic bytes as the fused step's)
     dom_bytes = disp_b if dom in ("dispatch_fused", "move_fused", "pack", "exchange", "deliver") else comb_b
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
-    traffic = traffic_for(dom, args.config)
+    traffic = traffic_for(dom, traffic_config(args, s, variant))
 
     e2e = None
     if not args.no_e2e and not variant:
@@ -600,7 +609,8 @@ def run_agrs(args):
     peak, peak_src = measured_peaks()
     n_tok = int(x.num_tokens.sum())
     achieved = total / (ms * 1e-3) / 1e9
-    tr = [traffic_for(k, args.config) for k in ("agrs_gather", "agrs_experts", "agrs_reduce")]
+    key = traffic_config(args, s)
+    tr = [traffic_for(k, key) for k in ("agrs_gather", "agrs_experts", "agrs_reduce")]
     traffic = sum(tr) if all(t is not None for t in tr) else None
     line = {
         "metric": METRIC, "value": n_tok / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": n,

@@ -65,6 +65,28 @@ def test_traffic_lookup_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("agrs_gather") == bench.kernel_source_hash("agrs_reduce")
 
 
+def test_traffic_only_for_the_unchanged_named_workload(tmp_path, monkeypatch):
+    src = bench.kernel_source_hash("dispatch_fused")
+    f = tmp_path / "traffic.txt"
+    f.write_text(f"kernel=dispatch_fused config=3 source={src} bytes_per_launch=123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+
+    def args(**kw):
+        d = dict(config=3, tokens_per_rank=None, experts=None, hidden=None, top_k=None)
+        d.update(kw)
+        return argparse.Namespace(**d)
+    a = args()
+    assert bench.traffic_config(a, bench.workload_spec(a)) == 3
+    assert bench.traffic_for("dispatch_fused", bench.traffic_config(a, bench.workload_spec(a))) == 123.0
+    # a smaller case of the same shape, or a variant, moves other bytes
+    for over in (dict(tokens_per_rank=256), dict(experts=64), dict(hidden=2048), dict(top_k=4)):
+        a = args(**over)
+        assert bench.traffic_config(a, bench.workload_spec(a)) is None
+    a = args()
+    assert bench.traffic_config(a, bench.workload_spec(a), {"x_dtype": "fp8"}) is None
+    assert bench.traffic_for("dispatch_fused", None) is None
+
+
 def test_variant_bookkeeping():
     base = argparse.Namespace(x_dtype="bf16", weight_on_input=False, ragged=False, zero_pad=False)
     assert bench.variant_of(base) == {}
