@@ -92,3 +92,16 @@ def test_variant_bookkeeping():
     assert bench.variant_of(base) == {}
     v = bench.variant_of(argparse.Namespace(x_dtype="fp8", weight_on_input=True, ragged=True, zero_pad=True))
     assert v["x_dtype"] == "fp8" and v["weight_on_input"] and v["zero_pad"] and "ragged" in v
+
+
+def test_cpu_baseline_all_cores_replicas():
+    r = bench.cpu_baseline_all_cores(1, budget_s=0.5, bytes_per_replica=1 << 28)
+    assert r is not None and r["value"] > 0 and r["cores"] >= 1
+    assert r["unit"] == bench.UNIT and "replicas" in r["sample"]
+
+
+def test_cpu_baseline_all_cores_reports_none_when_a_replica_fails():
+    import time
+    t0 = time.monotonic()
+    assert bench.cpu_baseline_all_cores(99, budget_s=0.5, bytes_per_replica=1 << 28) is None   # no workload 99
+    assert time.monotonic() - t0 < 120
