@@ -295,6 +295,7 @@ void oracle_combine(int W, int E, int K, int Tm, int h, const int32_t *num_token
                     const int64_t *row_off, int out_f32, void *out, const int64_t *tokens,
                     int64_t n_tokens) {
     int Ecap = Tm * W;
+    (void)E;   /* a flat row index needs only Ecap to split */
     float *acc = (float *)malloc(sizeof(float) * (size_t)h);
     int64_t n = tokens ? n_tokens : (int64_t)W * Tm;
     for (int64_t q = 0; q < n; ++q) {
