@@ -115,6 +115,36 @@ def test_edge_shapes(dev, W, E, K, T, h, pad, extras):
     _roundtrip(_custom(W, E, K, T, h, seed=W + E + T, pad=pad, extras=extras), dev, out_f32=(False, True))
 
 
+def _same_ids(W, E, K, T, h, row_ids, seed):
+    """Every token of every rank chooses the same experts (degenerate routing)."""
+    x = _custom(W, E, K, T, h, seed=seed)
+    x.topk_ids[:] = np.asarray(row_ids, np.int32)[None, None, :]
+    return x
+
+
+@pytest.mark.parametrize("path", ["fused", "sendbuf"])
+def test_one_expert_set_filled_to_capacity(dev, path):
+    """All tokens pick experts 0..3, all on rank 0: each of those experts receives
+    W * max_tokens rows, exactly its capacity, and every other rank receives none."""
+    W, E, K, T, h = 4, 16, 4, 200, 256
+    x = _same_ids(W, E, K, T, h, [0, 1, 2, 3], seed=11)
+    ctx, out, m = _roundtrip(x, dev, path=path, out_f32=(False, True),
+                             ctx_kw=dict(sendbuf=path == "sendbuf"))
+    ent = out.expert_num_tokens.cpu().numpy().reshape(W, E // W)
+    assert (ent[0] == W * T).all() and (ent[1:] == 0).all()
+    _check_two_stage(x, dev)
+
+
+def test_every_token_reaches_every_rank(dev):
+    """One expert per rank for every token (top_k = W): every token is sent to every
+    destination, so each (source, destination) block holds all T slots."""
+    W, E, K, T, h = 8, 64, 8, 130, 512
+    x = _same_ids(W, E, K, T, h, [d * 8 + (5 * d) % 8 for d in range(8)][::-1], seed=12)
+    ctx, out, m = _roundtrip(x, dev, out_f32=(False, True))
+    assert (m.send_cnt == T).all()
+    _check_two_stage(x, dev)
+
+
 def test_ragged_and_empty_ranks(dev):
     nt = np.array([0, 17, 128, 3, 64, 0, 127, 1], np.int32)
     x = _custom(8, 64, 8, 128, 256, seed=4, pad=0.05, num_tokens=nt)
