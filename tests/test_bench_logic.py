@@ -105,3 +105,29 @@ def test_cpu_baseline_all_cores_reports_none_when_a_replica_fails():
     t0 = time.monotonic()
     assert bench.cpu_baseline_all_cores(99, budget_s=0.5, bytes_per_replica=1 << 28) is None   # no workload 99
     assert time.monotonic() - t0 < 120
+
+
+def _run_bench(*argv, env=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    e = dict(os.environ, **(env or {}))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *argv], capture_output=True,
+                       text=True, timeout=300, env=e, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_line():
+    (d,) = _run_bench("--impl", "reference", "--config", "1", "--steps", "3", "--warmup", "1")
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny-w2-e8-k2-t16-h128"
+
+
+def test_reference_arm_prints_nothing_on_other_ranks():
+    assert _run_bench("--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "1",
+                      env={"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"}) == []
