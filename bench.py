@@ -371,16 +371,15 @@ def cpu_baseline_all_cores(cfg: int, budget_s: float = 8.0, bytes_per_replica: i
                       f"({sum(r[1] for r in res)} steps, {toks} tokens in {el:.1f} s)"}
 
 
-_REF_X = None
+_REF_X = {}
 
 
-def _ref_init(cfg: int, T: int):
-    global _REF_X
-    _REF_X = wl.make(wl.spec(cfg, T=T))
-
-
-def _ref_step(_):
-    return oracle_step(_REF_X)
+def _ref_step(arg):
+    cfg, T = arg
+    if (cfg, T) not in _REF_X:
+        _REF_X.clear()
+        _REF_X[(cfg, T)] = wl.make(wl.spec(cfg, T=T))
+    return oracle_step(_REF_X[(cfg, T)])
 
 
 def run_reference(args):
@@ -393,23 +392,28 @@ def run_reference(args):
     import multiprocessing as mp
     full = wl.spec(args.config)
     per_step_budget = min(0.25, 150.0 / max(1, args.steps + args.warmup))
-    # size the per-step sample: tokens per rank so one oracle step fits the budget
-    T = 8
-    x = wl.make(wl.spec(args.config, T=T))
-    t0 = time.perf_counter()
-    oracle_step(x)
-    dt = time.perf_counter() - t0
-    T = max(1, min(full.T, int(T * per_step_budget / max(dt, 1e-6))))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    per_replica = 4 * (4 << 30) * T // full.T + (1 << 30)   # ~2.5 GB at the full prefill step
+    per_replica = 4 << 30              # ~2.5 GB at the full prefill step, far less per sample
     n = max(1, min(cores, _host_memory_bytes() // 2 // per_replica))
-    with mp.get_context("spawn").Pool(n, initializer=_ref_init, initargs=(args.config, T)) as pool:
+    with mp.get_context("spawn").Pool(n) as pool:
+        def step(T):
+            return sum(pool.map(_ref_step, [(args.config, T)] * n, chunksize=1))
+        # size the per-step sample with every replica running: tokens per rank so one
+        # step of all replicas fits the budget (the first probe also loads the library)
+        T = min(32, full.T)
+        step(T)
+        dt = float("inf")
+        for _ in range(3):
+            t0 = time.perf_counter()
+            step(T)
+            dt = min(dt, time.perf_counter() - t0)
+        T = max(1, min(full.T, int(T * per_step_budget / max(dt, 1e-6))))
         for _ in range(args.warmup):
-            pool.map(_ref_step, range(n), chunksize=1)
+            step(T)
         toks = 0
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            toks += sum(pool.map(_ref_step, range(n), chunksize=1))
+            toks += step(T)
         el = time.perf_counter() - t0
     v = toks / el
     sample = (f"each step: {n} spawned replicas of the one-thread oracle, one per host core, "
