@@ -145,6 +145,34 @@ def test_every_token_reaches_every_rank(dev):
     _check_two_stage(x, dev)
 
 
+def test_side_streams_and_two_contexts(dev):
+    """Dispatch and combine are enqueued on the caller's current stream: two
+    contexts on two side streams, launched interleaved with no synchronisation
+    between them, each match the oracle (combine on identity experts)."""
+    xa = wl.make(2)
+    xb = _custom(4, 32, 4, 150, 1024, seed=21, pad=0.1)
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    runs = []
+    for x, st in zip((xa, xb), streams):
+        with torch.cuda.stream(st):
+            ctx = H.make_ctx(x, dev)
+            a1, ids, w, nt, extras = H.inputs_dev(x, dev)
+            out = ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras)
+        runs.append((x, ctx, out, a1, extras))
+    ys = []
+    for (x, ctx, out, a1, extras), st in zip(runs, streams):
+        with torch.cuda.stream(st):
+            ys.append(ctx.combine(out.b_a1))
+    torch.cuda.synchronize(dev)
+    for (x, ctx, out, a1, extras), y in zip(runs, ys):
+        ctx.check()
+        m = H.oracle_meta(x)
+        H.check_meta(ctx, m, x, out.expert_num_tokens)
+        H.check_rows(out, m, x, a1, extras)
+        exp = ref.combine(m, x.topk_weights, ref.dispatch_rows(m, x.a1))
+        assert np.array_equal(H.bits_host(y).reshape(exp.shape), exp)
+
+
 def test_ragged_and_empty_ranks(dev):
     nt = np.array([0, 17, 128, 3, 64, 0, 127, 1], np.int32)
     x = _custom(8, 64, 8, 128, 256, seed=4, pad=0.05, num_tokens=nt)
