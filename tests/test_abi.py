@@ -232,3 +232,20 @@ def test_agrs_host_checks(lib):
     assert call(buf=L.EpAgrsBuffersC(FAKE_WS, FAKE_WS, FAKE_WS, FAKE_WS + 4, None)) == L.EP_ERR_INVALID_ARG
     # W^2 * Tm * h / 8 work items must stay below 2^31
     assert call(c=cfg(W=64, E=64, K=8, T=8192, h=512)) == L.EP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c89"), ("c", "c99"), ("c", "c11"), ("c++", "c++17")])
+def test_header_compiles_alone_with_strict_warnings(tmp_path, lang, std):
+    """include/ep.h is plain C: it needs no CUDA or torch header and compiles
+    without a warning as C89 through C11 and as C++."""
+    import shutil
+    import subprocess
+    cc = "gcc" if lang == "c" else "g++"
+    if shutil.which(cc) is None:
+        pytest.skip(f"{cc} not available")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "ep.h"\nint main(void) { return EP_OK; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
