@@ -39,6 +39,9 @@
  *   - A context is used by one host thread at a time. Its dispatch and combine
  *     are ordered by the stream they are given; running one context on two
  *     streams at once races on its workspace.
+ *   - One device per process: a kernel's dynamic shared-memory limit is raised
+ *     on its first large launch in the process, for the device current then.
+ *     Drive several GPUs with one process each, as torchrun does.
  */
 #ifndef EP_H
 #define EP_H
