@@ -75,9 +75,26 @@ def workspace_bytes(cfg: EpConfig) -> int:
     return n.value
 
 
-def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+def _stream_ptr(stream: Optional[torch.cuda.Stream], dev: torch.device) -> int:
+    """The stream to enqueue on. The library launches on the current device, so
+    that must be the device the buffers live on, and a given stream must belong
+    to it: otherwise the kernels would address another device's memory."""
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError(f"the buffers are on {dev} but the current device is cuda:{cur}; "
+                         f"make {dev} current (torch.cuda.set_device) first")
     s = stream if stream is not None else torch.cuda.current_stream()
+    if s.device.index != cur:
+        raise ValueError(f"stream is on {s.device}, the buffers on {dev}")
     return s.cuda_stream
+
+
+def _cuda_device(device) -> torch.device:
+    """A CUDA device with its index filled in (the current device when absent)."""
+    d = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if d.type != "cuda":
+        raise ValueError(f"want a CUDA device, got {d}")
+    return d if d.index is not None else torch.device("cuda", torch.cuda.current_device())
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Sequence[int], dev) -> None:
@@ -101,7 +118,7 @@ class EpContext:
     def __init__(self, cfg: EpConfig, device: Optional[torch.device] = None,
                  workspace: Optional[torch.Tensor] = None):
         self.cfg = cfg
-        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.device = _cuda_device(device)
         self.tok_cap, self.slots, self.expert_cap = capacities(cfg)
         nbytes = workspace_bytes(cfg)
         if workspace is None:
@@ -166,7 +183,7 @@ class EpContext:
                                  topk_ids.data_ptr(), topk_weights.data_ptr(),
                                  ein if n_ex else None, out.b_a1.data_ptr(),
                                  eout if n_ex else None, out.expert_num_tokens.data_ptr(), p,
-                                 _stream_ptr(stream))
+                                 _stream_ptr(stream, dev))
         L.check(rc, "ep_dispatch")
         return out
 
@@ -181,7 +198,7 @@ class EpContext:
         _need(out, "out", out_dtype, (c.W, c.max_tokens, c.hidden), dev)
         code = {torch.bfloat16: L.EP_BF16, torch.float32: L.EP_F32}[out_dtype]
         L.check(L.lib().ep_combine(self._h, expert_out.data_ptr(), code, out.data_ptr(),
-                                   _stream_ptr(stream)), "ep_combine")
+                                   _stream_ptr(stream, dev)), "ep_combine")
         return out
 
     def combine_two_stage(self, expert_out: torch.Tensor, out: Optional[torch.Tensor] = None,
@@ -195,13 +212,13 @@ class EpContext:
         _need(out, "out", out_dtype, (c.W, c.max_tokens, c.hidden), dev)
         code = {torch.bfloat16: L.EP_BF16, torch.float32: L.EP_F32}[out_dtype]
         L.check(L.lib().ep_combine_two_stage(self._h, expert_out.data_ptr(), code, out.data_ptr(),
-                                             _stream_ptr(stream)), "ep_combine_two_stage")
+                                             _stream_ptr(stream, dev)), "ep_combine_two_stage")
         return out
 
     # ---------------------------------------------------------- utilities
     def status(self, stream: Optional[torch.cuda.Stream] = None) -> int:
         """Synchronise and return the device status code (0 = ok); clears it."""
-        return int(L.lib().ep_status(self._h, _stream_ptr(stream)))
+        return int(L.lib().ep_status(self._h, _stream_ptr(stream, self.device)))
 
     def check(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         L.check(self.status(stream), "device status")
@@ -302,5 +319,5 @@ def agrs(cfg: EpConfig, a1: torch.Tensor, topk_ids: torch.Tensor, topk_weights: 
                             a1.data_ptr(), topk_ids.data_ptr(), topk_weights.data_ptr(),
                             C.byref(buffers.to_c()),
                             L.EP_F32 if out_dtype == torch.float32 else L.EP_BF16,
-                            out.data_ptr(), _stream_ptr(stream)), "ep_agrs")
+                            out.data_ptr(), _stream_ptr(stream, dev)), "ep_agrs")
     return out

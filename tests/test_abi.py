@@ -249,3 +249,33 @@ def test_header_compiles_alone_with_strict_warnings(tmp_path, lang, std):
     r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
                         "-I", inc, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_binding_launches_only_on_the_buffers_device(monkeypatch):
+    """The binding refuses to enqueue when the current CUDA device (where the
+    library launches) is not the device the buffers live on, or when the given
+    stream belongs to another device: such a launch would address another
+    device's memory. Checked with a fake current device, no GPU needed."""
+    import torch
+    from combine_ep_route_gb300 import ep
+
+    class FakeStream:
+        def __init__(self, idx):
+            self.device = torch.device("cuda", idx)
+            self.cuda_stream = 1234 + idx
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: FakeStream(0))
+    assert ep._stream_ptr(None, torch.device("cuda", 0)) == 1234
+    assert ep._stream_ptr(FakeStream(0), torch.device("cuda", 0)) == 1234
+    with pytest.raises(ValueError, match="current device"):
+        ep._stream_ptr(None, torch.device("cuda", 1))
+    with pytest.raises(ValueError, match="current device"):
+        ep._stream_ptr(None, torch.device("cpu"))          # host buffers never reach a kernel
+    with pytest.raises(ValueError, match="stream is on"):
+        ep._stream_ptr(FakeStream(1), torch.device("cuda", 0))
+    assert ep._cuda_device(None) == torch.device("cuda", 0)
+    assert ep._cuda_device("cuda") == torch.device("cuda", 0)
+    assert ep._cuda_device(torch.device("cuda", 3)) == torch.device("cuda", 3)
+    with pytest.raises(ValueError):
+        ep._cuda_device("cpu")
