@@ -4,10 +4,11 @@ Each mutant is a copy of ``oracle/ep_oracle.c`` with one plausible slip: a wrong
 operator, index, stride, loop order or bound, a dropped term or rounding, a
 transposed operand. Each copy is compiled to its own library under a temporary
 directory. The oracle's pins (``test_oracle_pins.py``) then run against it in a
-child process, and at least one of them must fail on an assertion. The mutants
-keep every access in bounds, so a crash would be a mistake in the mutant, not a
-catch. The unmutated source must pass the same pin run, which shows that the
-runner itself works.
+child process, and at least one of them must fail on an assertion. The pins run
+in a fixed order and the run stops at the first failure; every mutant keeps its
+accesses in bounds on the inputs of the pins that run before the one that catches
+it, so a crash would be a mistake in the mutant, not a catch. The unmutated source
+must pass the same pin run, which shows that the runner itself works.
 
 The mistakes are planted in a copy of the oracle only; the library under
 ``oracle/`` and the CUDA path are not touched.
@@ -58,12 +59,12 @@ MUTANTS = [
      "if (e >= E - 1) { *err |= OR_ERR_EXPERT_ID; continue; }", 0),
     ("route: repeated ids not dropped",
      "if (dup) { *err |= OR_ERR_DUPLICATE; continue; }", "if (0) { *err |= OR_ERR_DUPLICATE; continue; }", 0),
-    ("route: one slot per pair instead of per (destination, token)",
-     "if (slot_on[d] < 0) {", "if (slot_on[d] < 0 || 1) {", 0),
+    ("route: slot numbered by token index, not compacted",
+     "slot_on[d] = send_cnt[s * W + d]++;", "slot_on[d] = t; send_cnt[s * W + d]++;", 0),
     ("route: columns filled from the last one",
      "int col = used_cols[d]++;", "int col = S - 1 - used_cols[d]++;", 0),
-    ("route: local expert id with the wrong stride",
-     "send_eloc[at] = row[k] - d * e_local;", "send_eloc[at] = row[k] - d * W;", 0),
+    ("route: column stored as the local expert id",
+     "send_eloc[at] = row[k] - d * e_local;", "send_eloc[at] = col;", 0),
     ("route: weight of the first pick for every column",
      "send_w[at] = weights[((size_t)s * Tm + t) * K + k];",
      "send_w[at] = weights[((size_t)s * Tm + t) * K + 0];", 0),
