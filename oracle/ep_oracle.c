@@ -29,9 +29,11 @@
  *     (the page sorts with an unstable argsort; its comment asks for the
  *     k-th expert in column k);
  *   - combine folds a token's experts in top-k order in fp32, one product and
- *     one sum per step, rounded once to the output type (parity unpinned in
- *     one respect: whether a product rounds before its sum; a fold that fuses
- *     them is also fp32 accumulation and no pin tells the two apart). The page sums
+ *     one sum per step, each rounded on its own (the page's finalize forms the
+ *     weighted rows as an fp32 tensor before it accumulates them, so a product
+ *     is rounded before it is added: no fused multiply-add), rounded once to
+ *     the output type. A hand-derived golden case pins both the separate
+ *     roundings and the top-k order of the fold. The page sums
  *     per-destination partials in fp32, rounds them to the activation type
  *     and sums those in the output type; `oracle_combine_pagemode` restates
  *     that two-stage form so tests can show both agree within tolerance;

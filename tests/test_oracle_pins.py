@@ -478,3 +478,50 @@ def test_agrs_worked_example_by_hand():
     single = wl.bf16_bits_to_f32(ref.combine(m, w, rows)).reshape(W, h)
     assert np.array_equal(single[0], np.array(g["expect_single_fold_bf16"], np.float32))
     assert np.array_equal(ref.combine_pagemode(m, rows), out)
+
+
+# ------------------------------------------- rounding of the combine fold, by hand
+
+def _fold_golden():
+    g = json.load(open(os.path.join(os.path.dirname(GOLDEN), "fold_rounding.json")))
+    W, E, K, Tm, h = g["W"], g["E"], g["K"], g["Tm"], g["h"]
+    ids = np.array(g["topk_ids"], np.int32)
+    w = np.array(g["topk_weights"], np.float64)
+    assert np.array_equal(w.astype(np.float32).astype(np.float64), w), "weights not fp32-exact"
+    a1f = np.array(g["a1"], np.float32)
+    a1 = wl.f32_to_bf16_bits(a1f)
+    assert np.array_equal(wl.bf16_bits_to_f32(a1), a1f), "a1 not bf16-exact"
+    nt = np.array(g["num_tokens"], np.int32)
+    expect = np.array(g["expect_out"], np.float32).reshape(W * Tm, h)
+    return g, W, E, K, Tm, h, ids, w.astype(np.float32), a1, nt, expect
+
+
+def _same_bits(got, expect):
+    got = np.asarray(got, np.float32)
+    return np.array_equal(got.view(np.uint32), expect.view(np.uint32))
+
+
+def test_fold_rounds_each_product_before_its_sum():
+    """tests/golden/fold_rounding.json: the page's finalize forms the weighted rows
+    as an fp32 tensor of their own and then accumulates them, so each product is
+    rounded before it is added. Hand-derived dyadic cases where a fused
+    multiply-add gives 2^-30 (or -2^-23, or one ulp more) instead of the separate
+    roundings' result, and one where the fold order shows; checked on the single
+    fold (both output types), the page's two-stage form and the all-gather /
+    reduce-scatter route, all with identity experts."""
+    g, W, E, K, Tm, h, ids, w, a1, nt, expect = _fold_golden()
+    m = ref.dispatch_meta(W, E, K, Tm, ids, w, nt)
+    assert m.err == 0
+    rows = ref.dispatch_rows(m, a1)        # identity experts: each pair's row is its token
+    out32 = ref.combine(m, w, rows, out_f32=True)
+    assert _same_bits(out32, expect), out32
+    outb = ref.combine(m, w, rows, out_f32=False)
+    assert _same_bits(wl.bf16_bits_to_f32(outb), expect)
+    for f32 in (False, True):
+        page = ref.combine_pagemode(m, rows, out_f32=f32)
+        page = page if f32 else wl.bf16_bits_to_f32(page)
+        assert _same_bits(page, expect), (f32, page)
+        ag, err = ref.agrs(W, E, K, Tm, a1, ids, w, nt, out_f32=f32)
+        assert err == 0
+        ag = ag if f32 else wl.bf16_bits_to_f32(ag)
+        assert _same_bits(ag, expect), (f32, ag)
