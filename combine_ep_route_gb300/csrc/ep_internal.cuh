@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ep.h"
+#include "smem_limit.h"
 
 namespace ep {
 
@@ -315,6 +316,19 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 
 // ------------------------------------------------------------- kernel launchers
+// Raise kernel fn's dynamic shared-memory limit to `bytes` on the current
+// device unless that (kernel, device) already has it (see smem_limit.h).
+inline cudaError_t ensure_dyn_smem(const void *fn, size_t bytes) {
+    if (bytes <= SmemLimits::kDefaultLimit) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return static_cast<cudaError_t>(smem_limits().ensure(fn, dev, bytes, [&] {
+        return static_cast<int>(
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+    }));
+}
+
 // Each returns the cudaError_t of the launch.
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 size_t route_smem_bytes(int n_ctr, int top_k);

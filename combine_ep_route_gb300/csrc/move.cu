@@ -437,13 +437,8 @@ __global__ void __launch_bounds__(256, 2) dispatch_fused_kernel(const RouteParam
 template <int KT>
 static cudaError_t launch_dispatch_fused_kt(const RouteParams &rp, const MoveParams &mp, int grid,
                                             size_t smem, cudaStream_t st) {
-    static size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_fused_kernel<KT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    cudaError_t e = ensure_dyn_smem((const void *)dispatch_fused_kernel<KT>, smem);
+    if (e != cudaSuccess) return e;
     dispatch_fused_kernel<KT><<<grid, kRouteThreads, smem, st>>>(rp, mp);
     return cudaGetLastError();
 }
@@ -464,7 +459,6 @@ cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, i
 
 cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size_t smem, bool pdl,
                         cudaStream_t st) {
-    static size_t smem_set[4] = {0, 0, 0, 0};
     const void *fn = nullptr;
     switch (mode) {
         case MOVE_FUSED: fn = (const void *)move_kernel<MOVE_FUSED>; break;
@@ -473,11 +467,8 @@ cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size
         case MOVE_DELIVER: fn = (const void *)move_kernel<MOVE_DELIVER>; break;
         default: return cudaErrorInvalidValue;
     }
-    if (smem > 48 * 1024 && smem > smem_set[mode]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set[mode] = smem;
-    }
+    cudaError_t se = ensure_dyn_smem(fn, smem);
+    if (se != cudaSuccess) return se;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);

@@ -47,13 +47,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
 
 template <int KT>
 static cudaError_t launch_route_kt(const RouteParams &p, size_t smem, cudaStream_t st) {
-    static size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<KT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    cudaError_t e = ensure_dyn_smem((const void *)route_kernel<KT>, smem);
+    if (e != cudaSuccess) return e;
     route_kernel<KT><<<p.num_tiles, kRouteThreads, smem, st>>>(p);
     return cudaGetLastError();
 }

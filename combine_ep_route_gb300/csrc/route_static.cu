@@ -17,6 +17,7 @@
 #include "ep_internal.cuh"
 
 #include <cstddef>
+#include <cstdint>
 #include <mutex>
 
 namespace {
@@ -47,6 +48,12 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
         !out->pair_send || !out->recv_eloc || !out->recv_w || !out->recv_row ||
         !out->expert_num_tokens)
         return EP_ERR_INVALID_ARG;
+    // every input and output is read or written as 4-byte words
+    const void *words[] = {num_tokens,      topk_ids,       topk_weights,   out->send_cnt,
+                           out->pair_row,   out->pair_w,    out->pair_send, out->recv_eloc,
+                           out->recv_w,     out->recv_row,  out->expert_num_tokens, out->status};
+    for (const void *p : words)
+        if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return EP_ERR_INVALID_ARG;
 
     // scratch this problem needs: header, tile flags, tile aggregates, tile prefixes
     const int W = cfg->W, Tm = cfg->max_tokens;
@@ -60,6 +67,9 @@ extern "C" int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens
     if (need > (size_t)EP_STATIC_SCRATCH_BYTES) return EP_ERR_SCRATCH_LIMIT;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the caller's status word says "no error" until the routing kernel has run
+    if (out->status && cudaMemsetAsync(out->status, 0, sizeof(int32_t), st) != cudaSuccess)
+        return EP_ERR_CUDA;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return EP_ERR_INVALID_ARG;

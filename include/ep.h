@@ -39,9 +39,11 @@
  *   - A context is used by one host thread at a time. Its dispatch and combine
  *     are ordered by the stream they are given; running one context on two
  *     streams at once races on its workspace.
- *   - One device per process: a kernel's dynamic shared-memory limit is raised
- *     on its first large launch in the process, for the device current then.
- *     Drive several GPUs with one process each, as torchrun does.
+ *   - Several devices: work goes to the device current when a call is made,
+ *     which must be the device of its buffers (a context's workspace binds it
+ *     to one device). The kernels' raised shared-memory limits are kept per
+ *     (kernel, device) under a lock, so one process may drive several GPUs
+ *     from one or several host threads.
  */
 #ifndef EP_H
 #define EP_H
@@ -131,16 +133,30 @@ int ep_workspace_bytes(const ep_config_t *cfg, size_t *bytes);
 
 /*
  * ep_ctx_create -- bind a context to cfg and to a caller-owned device
- * workspace of at least ep_workspace_bytes(cfg) bytes (256-byte aligned). The
- * context (host memory, freed by ep_ctx_destroy) keeps pointers only. The
- * workspace is initialised on first use, on the first dispatch's stream.
- * Touches no GPU. EP_ERR_INVALID_ARG for a bad config or null pointer,
- * EP_ERR_WORKSPACE for a small or misaligned workspace.
+ * workspace of at least ep_workspace_bytes(cfg) bytes (256-byte aligned).
+ * Counterpart of FlashInfer `MoeAlltoAll.__init__` (page
+ * flashinfer/comm/trtllm_moe_alltoall.py), which sizes a workspace per rank,
+ * takes it from `MoeAlltoAll.get_workspace` (a per-process cache,
+ * `_WORKSPACE_CACHE`, keyed by size, rank, EP size and max tokens) and starts
+ * in the idle phase of `_A2AState`. Here the caller allocates and owns the
+ * workspace (the library allocates no device memory) and may keep one per
+ * configuration as that cache does. The context (host memory, freed by
+ * ep_ctx_destroy) keeps pointers only and starts idle. The workspace is
+ * initialised on first use, on the first dispatch's stream. Touches no GPU.
+ * EP_ERR_INVALID_ARG for a bad config or null pointer, EP_ERR_WORKSPACE for a
+ * small or misaligned workspace.
  */
 int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_bytes,
                   ep_ctx_t **out);
 
-/* ep_ctx_destroy -- free the host context (not the workspace). NULL is a no-op. */
+/*
+ * ep_ctx_destroy -- free the host context (not the workspace, which the
+ * caller owns). NULL is a no-op. The FlashInfer page keeps its workspaces in
+ * `MoeAlltoAll._WORKSPACE_CACHE` for the life of the process and drops one only
+ * in `_reset_workspace`; here the caller frees the workspace once every
+ * context bound to it is destroyed and its last stream work has finished.
+ * Touches no GPU.
+ */
 int ep_ctx_destroy(ep_ctx_t *ctx);
 
 /*
@@ -216,15 +232,41 @@ int ep_combine_two_stage(ep_ctx_t *ctx, const void *expert_out, int32_t out_dtyp
  * ep_status -- synchronise the stream, then return and clear the first
  * device-side error recorded since the last call (EP_OK if none), or
  * EP_ERR_CUDA if the stream reports a CUDA error.
+ *
+ * The errors it reports are the checks FlashInfer's `MoeAlltoAll.dispatch` and
+ * `MoeAlltoAll.combine` make as asserts (runtime token count at most
+ * max_num_tokens; page flashinfer/comm/trtllm_moe_alltoall.py) plus the id
+ * checks the vLLM `prepare` leaves undefined (ids >= E, repeated ids; page
+ * fused_moe/prepare_finalize/alltoall_batched). Because those inputs live on
+ * the device, the checks run there and land in a status word. Reading it
+ * synchronises the host with the stream, which `prepare`'s rule of
+ * fixed-size collectives with no host sync avoids on purpose: ep_status is
+ * the one deliberate exception, for tests and debugging, and no other entry
+ * point calls it.
  */
 int ep_status(ep_ctx_t *ctx, void *stream);
 
-/* ep_ctx_reset -- return the context to idle (drops a dispatch that will not be combined). */
+/*
+ * ep_ctx_reset -- return the context to idle, dropping a dispatch that will
+ * not be combined. Counterpart of FlashInfer `MoeAlltoAll._reset_workspace`
+ * (page flashinfer/comm/trtllm_moe_alltoall.py), which the page keeps for
+ * testing: it synchronises, forgets the cached workspace and leaves the object
+ * unusable. Here the context stays usable and the workspace stays the
+ * caller's: only the `_A2AState` phase goes back to idle. Host only; touches
+ * no GPU and enqueues nothing.
+ */
 int ep_ctx_reset(ep_ctx_t *ctx);
 
 /*
  * Routing metadata kept in the workspace (device pointers; valid after a
- * dispatch has run). Filled by ep_get_metadata, which touches no GPU.
+ * dispatch has run). Filled by ep_get_metadata, which touches no GPU. It is
+ * this library's counterpart of FlashInfer's metainfo accessors
+ * (`MoeAlltoAll._init_constants`, `moe_a2a_get_metainfo_index_pairs`, page
+ * flashinfer/comm/trtllm_moe_alltoall.py), which name offsets into the
+ * workspace "for testing/debugging". The arrays are the combine context vLLM's
+ * `prepare` builds and `finalize` consumes (page
+ * fused_moe/prepare_finalize/alltoall_batched): per-destination counts, the
+ * received slots' local expert ids and weights, and where each pair landed.
  *   send_cnt  [W(s)][W(d)]          tokens rank s sends to rank d
  *   pair_row  [W][Tm][K]            flat b_a1 row (d*e_local+j)*Ecap+row of each pair, -1
  *   pair_w    [W][Tm][K]            router weight of each kept pair, 0 otherwise
@@ -252,6 +294,8 @@ typedef struct ep_metadata {
     int32_t reserved;
 } ep_metadata_t;
 
+/* ep_get_metadata -- fill *out (host) with the device addresses above. EP_ERR_INVALID_ARG
+ * for a null pointer. Host only. */
 int ep_get_metadata(const ep_ctx_t *ctx, ep_metadata_t *out);
 
 /* ep_error_string -- static text for a status code. */
@@ -322,8 +366,11 @@ typedef struct ep_route_outputs {
     float *recv_w;              /* [W(d)][W(s)][Tm][S] */
     int32_t *recv_row;          /* [W(d)][W(s)][Tm][S] */
     int32_t *expert_num_tokens; /* [W][e_local] */
-    int32_t *status;            /* [1] or NULL: set to 0 or to the call's first device-side
-                                   EP_ERR_* (bad id, repeated id, num_tokens out of range) */
+    int32_t *status;            /* [1] or NULL: cleared on the stream once the arguments
+                                   are accepted, then set to the call's first device-side
+                                   EP_ERR_* (bad id, repeated id, num_tokens out of range),
+                                   if any. Left untouched when the call returns an error
+                                   before that. */
 } ep_route_outputs_t;
 
 /*
@@ -356,8 +403,11 @@ typedef struct ep_route_outputs {
  * zero on its stream. Calls that overlap on the GPU (two streams, or two host
  * threads without ordering between their streams) race on the array.
  *
- * Host-side errors: EP_ERR_INVALID_ARG (bad config, null pointer),
- * EP_ERR_SCRATCH_LIMIT, EP_ERR_CUDA. Device-side errors go to out->status.
+ * Every pointer (inputs, outputs, status) must be 4-byte aligned.
+ *
+ * Host-side errors: EP_ERR_INVALID_ARG (bad config, null or misaligned
+ * pointer), EP_ERR_SCRATCH_LIMIT, EP_ERR_CUDA. Device-side errors go to
+ * out->status.
  */
 int ep_route_static(const ep_config_t *cfg, const int32_t *num_tokens, const int32_t *topk_ids,
                     const float *topk_weights, const ep_route_outputs_t *out, void *stream);

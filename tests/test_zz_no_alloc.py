@@ -28,12 +28,13 @@ def _cfg(s):
     return c
 
 
-def _existing(x, dev):
-    """Routing metadata through the existing entry point (ep_dispatch)."""
+def _existing(x, dev, expect_status=0):
+    """Routing metadata through the existing entry point (ep_dispatch), and the
+    device-side status ep_status reports for it."""
     ctx = H.make_ctx(x, dev)
     a1, ids, w, nt, extras = H.inputs_dev(x, dev)
     out = ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras)
-    ctx.check()
+    assert ctx.status() == expect_status
     got = {k: v.clone() for k, v in ctx.metadata().items() if k in KEYS}
     got["expert_num_tokens"] = out.expert_num_tokens.clone()
     ctx.reset()
@@ -94,6 +95,36 @@ def test_static_routing_matches_dispatch_on_two_calls_in_a_row():
     assert int(st_a.item()) == 0 and int(st_b.item()) == 0
     _same(xa, exp_a, got_a)
     _same(xb, exp_b, got_b)
+    # a third call: a ragged batch with one id repeated inside a token row; the
+    # status word must carry the code ep_status reports for the same inputs
+    xc = wl.make(wl.spec(2, T=96), num_tokens=np.array([96, 0, 17, 64, 95, 1, 50, 96], np.int32))
+    t = int(np.nonzero((xc.topk_ids[2, :17] >= 0).all(axis=1))[0][0])   # a routed token of rank 2
+    xc.topk_ids[2, t, 3] = xc.topk_ids[2, t, 1]
+    exp_c = _existing(xc, dev, expect_status=L.EP_ERR_DUPLICATE)
+    got_c, st_c, keep_c = _static_call(xc, dev)
+    torch.cuda.synchronize()
+    assert int(st_c.item()) == L.EP_ERR_DUPLICATE
+    _same(xc, exp_c, got_c)
+
+
+def test_static_routing_refuses_misaligned_pointers():
+    """Host-side check, no GPU work: one pointer off a 4-byte boundary at a time
+    is refused with EP_ERR_INVALID_ARG before anything is enqueued."""
+    from combine_ep_route_gb300 import build
+    build.build()
+    c = L.EpConfigC()
+    c.W, c.E, c.top_k, c.max_tokens, c.hidden, c.x_dtype = 2, 8, 2, 16, 64, L.EP_BF16
+    base = 0x7F0000000000
+    names = [f for f, _ in L.EpRouteOutputsC._fields_]
+    for bad in names + ["num_tokens", "topk_ids", "topk_weights"]:
+        o = L.EpRouteOutputsC()
+        for i, f in enumerate(names):
+            setattr(o, f, base + 0x100000 * (i + 1) + (2 if f == bad else 0))
+        nt = base + (2 if bad == "num_tokens" else 0)
+        ids = base + 0x40000000 + (2 if bad == "topk_ids" else 0)
+        w = base + 0x50000000 + (2 if bad == "topk_weights" else 0)
+        rc = L.lib().ep_route_static(C.byref(c), nt, ids, w, C.byref(o), None)
+        assert rc == L.EP_ERR_INVALID_ARG, bad
 
 
 def test_static_routing_refuses_problems_beyond_its_scratch():
