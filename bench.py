@@ -73,6 +73,10 @@ def parse():
     ap.add_argument("--hot", action="store_true",
                     help="no L2 flush between timed steps: the L2-resident figure of a small "
                          "workload, reported beside the flushed one, never as the headline")
+    ap.add_argument("--probe", default=None, choices=["ceilings"],
+                    help="ceilings: auxiliary line with the device's read-only, write-only and copy "
+                         "bandwidth (1 GiB buffers, torch's own kernels) and the host link's copy "
+                         "rates (pinned 118 MiB buffers); changes no GPU setting")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -217,6 +221,98 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event (throttle) reasons read through NVML's
+    read-only queries every ~1 ms on a background thread, so that even a timed
+    region of a few milliseconds holds several samples. ``mark()`` opens and
+    closes named windows (the timed passes); ``summary(name)`` describes the
+    samples inside one. Nothing here changes any GPU setting. Falls back to
+    None when the NVML library cannot be loaded."""
+    # clock-event reason bits of NVML's public API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int, interval_s: float = 0.001):
+        import ctypes
+        import threading
+        self.ok = False
+        self.samples = []          # (t, sm_mhz, reasons_mask, power_mw)
+        self.windows = {}
+        self.interval = interval_s
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = cuda_index
+            parts = [p.strip() for p in vis.split(",") if p.strip()]
+            if parts and all(p.isdigit() for p in parts) and cuda_index < len(parts):
+                idx = int(parts[cuda_index])
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                return
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self._lib, self._h, self._ct = lib, h, ctypes
+            self.ok = True
+        except Exception:
+            return
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        ct, lib, h = self._ct, self._lib, self._h
+        clk, rs, pw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            a = lib.nvmlDeviceGetClockInfo(h, ct.c_int(1), ct.byref(clk))
+            b = self._reasons_fn(h, ct.byref(rs))
+            c = lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw))
+            if a == 0:
+                self.samples.append((t, float(clk.value), int(rs.value) if b == 0 else None,
+                                     int(pw.value) if c == 0 else None))
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self.ok:
+            self._thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 2.0:
+                time.sleep(0.001)
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._thread.join(timeout=2)
+
+    def mark(self, name: str, start: bool):
+        w = self.windows.setdefault(name, [None, None])
+        w[0 if start else 1] = time.perf_counter()
+
+    def summary(self, name: str):
+        if not self.ok:
+            return None
+        t0, t1 = self.windows.get(name, (None, None))
+        sel = [x for x in list(self.samples) if t0 is not None and t1 is not None and t0 <= x[0] <= t1]
+        reasons = set()
+        for _, _, m, _ in sel:
+            for bit, n in self.REASONS.items():
+                if m is not None and m & bit:
+                    reasons.add(n)
+        pw = [x[3] / 1000.0 for x in sel if x[3] is not None]
+        sm = [x[1] for x in sel]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sel),
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(pw) if pw else None,
+                "window_ms": (t1 - t0) * 1e3 if t0 is not None and t1 is not None else None,
+                "source": "NVML read-only queries every ~1 ms on a host thread"}
 
 
 def replica_aggregate(ms_local: float, tokens_local: int, dist=None, device=None):
@@ -382,32 +478,34 @@ def _ref_step(arg):
     return oracle_step(_REF_X[(cfg, T)])
 
 
-def run_reference(args):
+def run_reference(args, budget_s: float = 200.0):
     """The oracle, unchanged, on the host cores: one spawned replica per core
-    (fewer if memory is short), each step every replica running one oracle step
-    on a token sample of the workload sized so the whole run ends in minutes."""
+    (fewer if memory is short), each step every replica running one oracle step.
+    Each replica runs the full workload when warm-up plus timed steps fit in
+    about budget_s; otherwise a token sample of it, sized so the run ends in
+    minutes, and the line's config names the sampled tokens per rank."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     import multiprocessing as mp
     full = wl.spec(args.config)
-    per_step_budget = min(0.25, 150.0 / max(1, args.steps + args.warmup))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     per_replica = 4 << 30              # ~2.5 GB at the full prefill step, far less per sample
     n = max(1, min(cores, _host_memory_bytes() // 2 // per_replica))
+    n_steps = max(1, args.steps + args.warmup)
     with mp.get_context("spawn").Pool(n) as pool:
         def step(T):
             return sum(pool.map(_ref_step, [(args.config, T)] * n, chunksize=1))
-        # size the per-step sample with every replica running: tokens per rank so one
-        # step of all replicas fits the budget (the first probe also loads the library)
-        T = min(32, full.T)
-        step(T)
-        dt = float("inf")
-        for _ in range(3):
-            t0 = time.perf_counter()
+        # one full step with every replica running (the first call also loads the
+        # library and draws the inputs, so time a second one)
+        step(full.T)
+        t0 = time.perf_counter()
+        step(full.T)
+        dt_full = time.perf_counter() - t0
+        T = full.T
+        if dt_full * n_steps > budget_s:
+            T = max(1, min(full.T, int(full.T * budget_s / n_steps / dt_full)))
             step(T)
-            dt = min(dt, time.perf_counter() - t0)
-        T = max(1, min(full.T, int(T * per_step_budget / max(dt, 1e-6))))
         for _ in range(args.warmup):
             step(T)
         toks = 0
@@ -416,15 +514,16 @@ def run_reference(args):
             toks += step(T)
         el = time.perf_counter() - t0
     v = toks / el
-    sample = (f"each step: {n} spawned replicas of the one-thread oracle, one per host core, "
-              f"each on {full.name} with {T} tokens per rank ({full.W * T} tokens, same "
-              f"generators)")
+    same = T == full.T
+    sample = (f"each step: {n} spawned replicas of the one-thread oracle, one per host core, each "
+              f"one step of {full.name} " + ("(the full workload)" if same else
+                                            f"on a sample of {T} tokens per rank (same generators)"))
+    cfg = {"workload": full.name if same else f"{full.name}-sample-T{T}", "W": full.W, "E": full.E,
+           "top_k": full.K, "tokens_per_rank": T, "hidden": full.h, "path": "oracle"}
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": full.name, "W": full.W, "E": full.E, "top_k": full.K,
-                       "tokens_per_rank": full.T, "hidden": full.h, "path": "oracle"},
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -532,9 +631,17 @@ def run_ours(args):
         return [a.elapsed_time(b) for a, b in ev], t_wall
 
     # 1. the headline: K steps, nothing but the library's kernels between the step events
-    with ClockSampler(local) as clk:
+    nv = NvmlSampler(local)
+    nv.__enter__()
+    if nv.ok:
+        nv.mark("headline", True)
         step_ms, t_wall = timed_region()
-    clocks = clk.summary()
+        nv.mark("headline", False)
+        clocks = nv.summary("headline")
+    else:
+        with ClockSampler(local) as clk:
+            step_ms, t_wall = timed_region()
+        clocks = clk.summary()
     launches = int(sum(v[0] for v in ctx.kernel_times().values()))
     if args.graph:   # replays do not pass through the host API: count the captured kernels
         launches = n * per_step_launches
@@ -542,7 +649,9 @@ def run_ours(args):
     # 2. per-kernel durations for the roofline: K more steps with CUDA events around
     #    every kernel launch, on the launching stream
     ctx.set_option(L.EP_OPT_KERNEL_TIMING, 1)
+    nv.mark("per_kernel", True)
     step_ms_ev, _ = timed_region()
+    nv.mark("per_kernel", False)
     kt = ctx.kernel_times()
     ctx.set_option(L.EP_OPT_KERNEL_TIMING, 0)
     # 3. medians of dispatch and combine timed separately (events around each call,
@@ -550,6 +659,7 @@ def run_ours(args):
     reps = 200
     evm = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
     torch.cuda.synchronize()
+    nv.mark("separate_calls", True)
     for i in range(reps):
         if not args.hot:
             flush.zero_()
@@ -559,6 +669,10 @@ def run_ours(args):
         combine(expert_out, out=y)
         evm[i][2].record(stream)
     torch.cuda.synchronize()
+    nv.mark("separate_calls", False)
+    nv.__exit__()
+    if nv.ok:
+        clocks["other_passes"] = {k: nv.summary(k) for k in ("per_kernel", "separate_calls")}
     med_d = float(np.median([e[0].elapsed_time(e[1]) for e in evm]))
     med_c = float(np.median([e[1].elapsed_time(e[2]) for e in evm]))
     disp_b, comb_b = algorithmic_bytes(x, x_row_bytes=cfg.x_row_bytes, extra_bytes=sum(extra_row_bytes))
@@ -796,9 +910,71 @@ def run_e2e(ctx, x, dev, out, n, stream, combine=None):
                    "copied back every step on separate streams (double-buffered)"}
 
 
+def run_ceilings(args):
+    """Reference points for the roofline discussion, not the roofline's denominator
+    (that is the measured copy peak): how fast plain read-only, write-only
+    and copy kernels move 1 GiB on this GPU, and how fast the host link copies.
+    CUDA events on the stream that launches each op; best and median of 10."""
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n = 1 << 30
+    a = torch.ones(n // 4, dtype=torch.int32, device=dev)
+    b = torch.empty(n // 4, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+
+    def timed(fn, nbytes, reps=10, streams=None):
+        ms = []
+        for i in range(reps + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(st)
+            fn()
+            for s2 in streams or ():
+                st.wait_stream(s2)
+            e1.record(st)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ms.append(e0.elapsed_time(e1))
+        return {"best_gbs": nbytes / (min(ms) * 1e-3) / 1e9,
+                "median_gbs": nbytes / (float(np.median(ms)) * 1e-3) / 1e9, "bytes": nbytes}
+
+    out = {"probe": "ceilings", "device": torch.cuda.get_device_name(dev),
+           "read_only": timed(lambda: a.max(), n),
+           "write_only": timed(lambda: b.zero_(), n),
+           "copy": timed(lambda: b.copy_(a), 2 * n)}
+    del a, b
+    m = 118 << 20
+    h_src = torch.ones(m, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(m, dtype=torch.uint8).pin_memory()
+    d_src = torch.ones(m, dtype=torch.uint8, device=dev)
+    d_dst = torch.empty(m, dtype=torch.uint8, device=dev)
+    s_up, s_dn = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def both():
+        s_up.wait_stream(st)
+        s_dn.wait_stream(st)
+        with torch.cuda.stream(s_up):
+            d_dst.copy_(h_src, non_blocking=True)
+        with torch.cuda.stream(s_dn):
+            h_dst.copy_(d_src, non_blocking=True)
+
+    out["host_to_device"] = timed(lambda: d_dst.copy_(h_src, non_blocking=True), m)
+    out["device_to_host"] = timed(lambda: h_dst.copy_(d_src, non_blocking=True), m)
+    out["both_directions"] = timed(both, 2 * m, streams=(s_up, s_dn))
+    out["note"] = ("read_only: int32 max over 1 GiB; write_only: zero_ of 1 GiB; copy: copy_ of "
+                   "1 GiB (read + write bytes); host link: cudaMemcpyAsync through torch on "
+                   "pinned 118 MiB buffers, both directions on two streams at once")
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.probe == "ceilings":
+        run_ceilings(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.route == "agrs":
         run_agrs(args)

@@ -126,6 +126,8 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny-w2-e8-k2-t16-h128"
+    # the whole run fits the budget, so every step is the full workload
+    assert d["config"]["tokens_per_rank"] == 16 and "full workload" in d["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_prints_nothing_on_other_ranks():
