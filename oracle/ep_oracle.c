@@ -43,7 +43,12 @@
  *     sum rounded for bf16 output, fp32 sums for fp32 output).
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no FMA contraction, so each
- * product and each sum rounds on its own, as the fold above states).
+ * product and each sum rounds on its own, as the fold above states). A second
+ * build with -fopenmp serves only to time the oracle on all host cores: its
+ * pragmas split the row copies and the combine over independent (rank, rank),
+ * expert or token blocks. Every output element is still computed by one thread
+ * in the order written here, so both builds give identical results; without
+ * -fopenmp the pragmas are ignored.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -227,6 +232,7 @@ void oracle_pair_rows(int W, int E, int K, int Tm, const int32_t *expert_num_tok
 void oracle_pack(int W, int Tm, size_t rb, const int32_t *send_cnt, const int32_t *send_tok,
                  const uint8_t *src_rows, uint8_t *send_x) {
     memset(send_x, 0, (size_t)W * W * Tm * rb);
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int s = 0; s < W; ++s)
         for (int d = 0; d < W; ++d)
             for (int slot = 0; slot < send_cnt[s * W + d]; ++slot) {
@@ -239,6 +245,7 @@ void oracle_pack(int W, int Tm, size_t rb, const int32_t *send_cnt, const int32_
 /* The payload all_to_all_single: recv_x[d][s] = send_x[s][d]. */
 void oracle_exchange(int W, int Tm, size_t rb, const uint8_t *send_x, uint8_t *recv_x) {
     size_t blk = (size_t)Tm * rb;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int s = 0; s < W; ++s)
         for (int d = 0; d < W; ++d)
             memcpy(recv_x + ((size_t)d * W + s) * blk, send_x + ((size_t)s * W + d) * blk, blk);
@@ -252,6 +259,7 @@ void oracle_deliver(int W, int E, int Tm, size_t rb, const int32_t *expert_num_t
                     uint8_t *out_rows) {
     int e_local = E / W;
     int Ecap = Tm * W;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int d = 0; d < W; ++d)
         for (int j = 0; j < e_local; ++j) {
             int n = expert_num_tokens[d * e_local + j];
@@ -300,8 +308,11 @@ void oracle_combine(int W, int E, int K, int Tm, int h, const int32_t *num_token
                     int64_t n_tokens) {
     int Ecap = Tm * W;
     (void)E;   /* a flat row index needs only Ecap to split */
-    float *acc = (float *)malloc(sizeof(float) * (size_t)h);
     int64_t n = tokens ? n_tokens : (int64_t)W * Tm;
+#pragma omp parallel
+    {
+    float *acc = (float *)malloc(sizeof(float) * (size_t)h);
+#pragma omp for schedule(static)
     for (int64_t q = 0; q < n; ++q) {
         int64_t g = tokens ? tokens[q] : q;
         int s = (int)(g / Tm), t = (int)(g % Tm);
@@ -327,6 +338,7 @@ void oracle_combine(int W, int E, int K, int Tm, int h, const int32_t *num_token
         }
     }
     free(acc);
+    }
 }
 
 /*

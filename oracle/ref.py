@@ -24,12 +24,22 @@ ERR_DUPLICATE = 2
 ERR_CAPACITY = 4
 
 _lib = None
+_openmp = False
+
+
+def use_openmp(on: bool = True) -> None:
+    """Load the -fopenmp build of the same oracle source from the next call on
+    (for timing on all host cores; results are identical). Call it before the
+    first oracle call of the process."""
+    global _lib, _openmp
+    _openmp = bool(on)
+    _lib = None
 
 
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(_build.build())
+        _lib = C.CDLL(_build.build(openmp=_openmp))
         P = C.c_void_p
         i = C.c_int
         _lib.oracle_capacities.argtypes = [i, i, i, i, P, P, P]
