@@ -77,6 +77,9 @@ def parse():
                     help="ceilings: auxiliary line with the device's read-only, write-only and copy "
                          "bandwidth (1 GiB buffers, torch's own kernels) and the host link's copy "
                          "rates (pinned 118 MiB buffers); changes no GPU setting")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a library option (EP_OPT_<NAME>) on the context before timing, "
+                         "e.g. --option PDL=1; named in the line's config")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -122,7 +125,8 @@ def measured_peaks():
 
 # translation unit of each timed kernel; its hash also covers every shared header
 # and api.cu, which sets the kernel's launch shape
-KERNEL_TU = {"dispatch_fused": "move.cu", "move_fused": "move.cu", "pack": "move.cu",
+KERNEL_TU = {"dispatch_fused": "move.cu", "dispatch_small": "dispatch_small.cu",
+             "move_fused": "move.cu", "pack": "move.cu",
              "exchange": "move.cu", "deliver": "move.cu", "route": "route.cu",
              "combine": "combine.cu", "combine_two_stage": "combine.cu", "zero_pad": "combine.cu",
              "agrs_gather": "agrs.cu", "agrs_experts": "agrs.cu", "agrs_reduce": "agrs.cu"}
@@ -356,6 +360,8 @@ def variant_of(args) -> dict:
         v["ragged"] = "num_tokens ~ U[T/2, T] per rank, seed 7"
     if args.zero_pad:
         v["zero_pad"] = True
+    if getattr(args, "option", None):
+        v["options"] = sorted(args.option)
     return v
 
 
@@ -467,6 +473,58 @@ def cpu_baseline_all_cores(cfg: int, budget_s: float = 8.0, bytes_per_replica: i
                       f"({sum(r[1] for r in res)} steps, {toks} tokens in {el:.1f} s)"}
 
 
+def _oracle_omp_child(cfg: int, budget_s: float, threads: int, out):
+    os.environ["OMP_NUM_THREADS"] = str(threads)
+    try:
+        from oracle import ref
+        ref.use_openmp(True)
+        x = wl.make(cfg)
+        oracle_step(x)                 # untimed: builds/loads the library, pages buffers in
+        toks, reps, t0 = 0, 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s and reps < 64:
+            toks += oracle_step(x)
+            reps += 1
+        out.put((toks, reps, time.perf_counter() - t0))
+    except BaseException as e:         # report, never hang the parent
+        out.put(("error", repr(e)))
+
+
+def cpu_baseline_openmp(cfg: int, budget_s: float = 8.0):
+    """The oracle's OpenMP build (same source, same results) on all host cores:
+    one full step at a time, its row copies and combine split over the cores,
+    its routing on one thread, repeated for about budget_s. Throughput = tokens
+    over wall time, so one step's latency is ms_per_step."""
+    import multiprocessing as mp
+    import queue
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    pr = ctx.Process(target=_oracle_omp_child, args=(cfg, budget_s, cores, out))
+    pr.start()
+    r, deadline = None, time.monotonic() + budget_s + 600
+    while r is None and time.monotonic() < deadline:
+        try:
+            r = out.get(timeout=1.0)
+        except queue.Empty:
+            if pr.exitcode is not None:     # ended without a result
+                try:
+                    r = out.get(timeout=1.0)
+                except queue.Empty:
+                    pass
+                break
+    pr.join(timeout=30)
+    if pr.is_alive():
+        pr.terminate()
+        pr.join()
+    if not r or r[0] == "error":
+        return None
+    toks, reps, el = r
+    return {"value": toks / el, "unit": UNIT, "cores": cores, "ms_per_step": el / reps * 1e3,
+            "kind": "oracle, OpenMP build (copies and combine over all cores, routing on one)",
+            "sample": f"{reps} full step(s) of {wl.spec(cfg).name} ({toks} tokens) in {el:.1f} s, "
+                      f"one step at a time on {cores} threads"}
+
+
 _REF_X = {}
 
 
@@ -566,6 +624,9 @@ def run_ours(args):
                    sendbuf=args.path == "sendbuf" or args.combine == "two_stage",
                    x_dtype=args.x_dtype, weight_on_input=args.weight_on_input, zero_pad=args.zero_pad)
     ctx = EpContext(cfg, dev)
+    for o in getattr(args, "option", None) or []:
+        name, val = o.split("=", 1)
+        ctx.set_option(getattr(L, "EP_OPT_" + name.strip().upper()), int(val))
     if quant:
         a1 = torch.from_numpy(a1_host).to(dev).view(cfg.x_torch_dtype)
         extras = [torch.from_numpy(e).to(dev) for e in extra_host]
@@ -682,16 +743,17 @@ def run_ours(args):
     # per-kernel durations (CUDA events around every launch, on the launch stream)
     per = {}
     for name in ("route", "move_fused", "pack", "exchange", "deliver", "combine", "combine_two_stage",
-                 "dispatch_fused"):
+                 "dispatch_fused", "dispatch_small"):
         _, tot, timed = kt[name]
         if timed:
             per[name] = tot / timed
-    cands = [k for k in ("dispatch_fused", "move_fused", "pack", "exchange", "deliver", "combine",
-                         "combine_two_stage") if k in per]
+    cands = [k for k in ("dispatch_fused", "dispatch_small", "move_fused", "pack", "exchange", "deliver",
+                         "combine", "combine_two_stage") if k in per]
     dom = max(cands, key=lambda k: per[k])
     # algorithmic bytes of one launch of the dominant kernel (send-buffer steps and the
     # two-stage combine are charged the same algorithmic bytes as the fused step's)
-    dom_bytes = disp_b if dom in ("dispatch_fused", "move_fused", "pack", "exchange", "deliver") else comb_b
+    dom_bytes = disp_b if dom in ("dispatch_fused", "dispatch_small", "move_fused", "pack", "exchange",
+                                  "deliver") else comb_b
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
     traffic = traffic_for(dom, traffic_config(args, s, variant))
 
@@ -701,7 +763,8 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not variant:
         cpu = cpu_baseline(args.config)
-        cpu["all_cores"] = cpu_baseline_all_cores(args.config)
+        cpu["all_cores"] = cpu_baseline_openmp(args.config)
+        cpu["replicas"] = cpu_baseline_all_cores(args.config)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n,

@@ -52,12 +52,13 @@ EP_OPT_MOVE_CHUNK_BYTES = 8
 EP_OPT_MOVE_MAX_STAGES = 9
 EP_OPT_FUSED_DISPATCH = 10
 EP_OPT_ROUTE_CTAS = 11
+EP_OPT_SMALL_DISPATCH = 12
 
 (EP_K_ROUTE, EP_K_MOVE_FUSED, EP_K_PACK, EP_K_EXCHANGE, EP_K_DELIVER, EP_K_COMBINE, EP_K_ZERO_PAD,
- EP_K_COMBINE_TWO_STAGE, EP_K_DISPATCH_FUSED) = range(9)
-EP_K_COUNT = 9
+ EP_K_COMBINE_TWO_STAGE, EP_K_DISPATCH_FUSED, EP_K_DISPATCH_SMALL) = range(10)
+EP_K_COUNT = 10
 KERNEL_NAMES = ("route", "move_fused", "pack", "exchange", "deliver", "combine", "zero_pad",
-                "combine_two_stage", "dispatch_fused")
+                "combine_two_stage", "dispatch_fused", "dispatch_small")
 
 
 class EpConfigC(C.Structure):

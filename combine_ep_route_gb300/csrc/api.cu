@@ -124,6 +124,7 @@ struct ep_ctx {
     int route_ctas;          // CTAs of that launch that route (0 = all, -1 = chosen per problem)
     int move_chunk_target;   // bytes; 0 = whole rows, -1 = chosen per problem
     int move_max_stages;     // -1 = chosen per problem (as move_pipes)
+    int small_dispatch;      // small batches: the one-launch dispatch without waits (-1 auto, 0 off)
     // counters and event timing
     int64_t launches[EP_K_COUNT];
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[EP_K_COUNT];
@@ -151,7 +152,7 @@ cudaEvent_t take_event(ep_ctx *c) {
 // Records an event pair around one kernel launch when timing is on.
 const char *const kKindRange[EP_K_COUNT] = {
     "ep:route", "ep:move_fused", "ep:pack", "ep:exchange", "ep:deliver",
-    "ep:combine", "ep:zero_pad", "ep:combine_two_stage", "ep:dispatch_fused"};
+    "ep:combine", "ep:zero_pad", "ep:combine_two_stage", "ep:dispatch_fused", "ep:dispatch_small"};
 
 // Around every library launch: a launch count, an NVTX range named for the
 // kernel (visible to Nsight tools; free when none is attached) and, with
@@ -344,6 +345,26 @@ int auto_route_ctas(const ep_ctx *c) {
     return need > 32.0 ? (int)need + 1 : 32;
 }
 
+// Token slots per CTA of the small-batch dispatch (dispatch_small.cu), or 0
+// when the batch does not qualify: its ids must be few enough for every CTA to
+// read (W * max_tokens * top_k <= kSmallMaxIds), one CTA per SM must cover the
+// slots with at most kSmallMaxTokens each, and their rows must fit in shared
+// memory. Needs num_sms (set on first use).
+int small_n_per(const ep_ctx *c, uint32_t *stage_bytes, size_t *smem) {
+    if (c->small_dispatch == 0 || c->num_sms < 1) return 0;
+    const ep_config_t &cf = c->cfg;
+    const long long slots = (long long)cf.W * cf.max_tokens;
+    if (slots * cf.top_k > ep::kSmallMaxIds) return 0;
+    const long long n_per = (slots + c->num_sms - 1) / c->num_sms;
+    if (n_per > ep::kSmallMaxTokens) return 0;
+    const uint32_t sb = (uint32_t)align_up(c->L.row_bytes, 128);
+    const size_t bytes = ep::small_smem_bytes((int)n_per, sb, c->L.n_ctr, cf.top_k, cf.W);
+    if (bytes > ep::kMoveSmemBudget) return 0;
+    *stage_bytes = sb;
+    *smem = bytes;
+    return (int)n_per;
+}
+
 int launch_move_mode(ep_ctx *c, int mode, int kind, const void *a1, const void *const *extra_in,
                      void *b_a1, void *const *extra_out, bool pdl, cudaStream_t st) {
     ep::MoveParams m;
@@ -423,6 +444,7 @@ int ep_ctx_create(const ep_config_t *cfg, void *d_workspace, size_t workspace_by
     c->route_ctas = -1;
     c->move_chunk_target = -1;
     c->move_max_stages = -1;
+    c->small_dispatch = -1;
     for (int k = 0; k < EP_K_COUNT; ++k) c->launches[k] = 0;
     *out = c;
     return EP_OK;
@@ -492,6 +514,10 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value) {
         case EP_OPT_ROUTE_CTAS:
             if (value < -1 || value > 4096) return EP_ERR_INVALID_ARG;
             ctx->route_ctas = (int)value;
+            return EP_OK;
+        case EP_OPT_SMALL_DISPATCH:
+            if (value < -1 || value > 1) return EP_ERR_INVALID_ARG;
+            ctx->small_dispatch = (int)value;
             return EP_OK;
         default: return EP_ERR_INVALID_ARG;
     }
@@ -588,7 +614,29 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         ctx->move_ctas_per_sm = saved_ctas;
         one_launch = fblock <= ep::kRouteThreads;
     }
-    if (one_launch) {
+    uint32_t small_sb = 0;
+    size_t small_smem = 0;
+    const int small = one_launch ? small_n_per(ctx, &small_sb, &small_smem) : 0;
+    if (small > 0) {
+        ep::SmallParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.rp = rp;
+        fill_move_common(ctx, sp.mp);
+        sp.mp.src_seg[0] = static_cast<const uint8_t *>(a1);
+        sp.mp.dst_seg[0] = static_cast<uint8_t *>(b_a1);
+        for (int i = 0; i < cf.n_extra; ++i) {
+            sp.mp.src_seg[1 + i] = static_cast<const uint8_t *>(extra_in[i]);
+            sp.mp.dst_seg[1 + i] = static_cast<uint8_t *>(extra_out[i]);
+        }
+        sp.n_per = small;
+        sp.stage_bytes = small_sb;
+        sp.div_tm = ep::make_fastdiv((uint32_t)cf.max_tokens);
+        sp.div_el = ep::make_fastdiv((uint32_t)L.e_local);
+        const int slots = cf.W * cf.max_tokens;
+        const int grid = (slots + small - 1) / small;
+        KernelTimer tm(ctx, EP_K_DISPATCH_SMALL, st);
+        if (ep::launch_dispatch_small(sp, grid, small_smem, st) != cudaSuccess) return EP_ERR_CUDA;
+    } else if (one_launch) {
         fm.wait_tiles = 1;
         fm.dynamic_units = 1;
         fm.tile_flag = rp.tile_flag;

@@ -118,6 +118,19 @@ struct MoveParams {
     FastDiv div_tm;
 };
 
+// One-launch dispatch of a small batch (dispatch_small.cu): every CTA owns
+// n_per consecutive token slots and counts its own prefix.
+constexpr int kSmallMaxTokens = 32;    // token slots per CTA, at most (one lane bit each)
+constexpr int kSmallMaxIds = 16384;    // W * max_tokens * top_k, at most (ids every CTA may read)
+
+struct SmallParams {
+    RouteParams rp;          // routing inputs and outputs (the tile fields are unused)
+    MoveParams mp;           // payload segments (the pipeline fields are unused)
+    int n_per;               // token slots per CTA, 1..kSmallMaxTokens
+    uint32_t stage_bytes;    // shared memory per token row (segments at seg_off)
+    FastDiv div_tm, div_el;  // division by max_tokens and by e_local
+};
+
 struct CombineParams {
     const uint8_t *expert_out;   // [E*Ecap][h] bf16
     const int32_t *pair_row;
@@ -337,6 +350,8 @@ cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size
 // Routing and the fused row movement in one persistent launch (grid = resident CTAs).
 cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, int grid,
                                   size_t move_smem, cudaStream_t st);
+size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W);
+cudaError_t launch_dispatch_small(const SmallParams &sp, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st);
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);

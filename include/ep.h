@@ -326,6 +326,11 @@ const char *ep_error_string(int code);
                                      0 = every CTA routes first; -1 (default) = chosen per
                                      problem: 0 up to 32 routing tiles, else enough routers to
                                      stay ahead of the row movers, at least 32 (-1..4096) */
+#define EP_OPT_SMALL_DISPATCH 12  /* fused path on a small batch (W * max_tokens * top_k at most
+                                     16384, at most 32 token slots per SM): one launch in which
+                                     every CTA counts its own tokens' prefix from the earlier
+                                     tokens' ids, with no waiting between CTAs. -1 (default) =
+                                     used whenever the batch qualifies, 0 = never, 1 = as -1 */
 
 /* ep_set_option -- set one EP_OPT_* value (host only). EP_ERR_INVALID_ARG for an unknown option or value. */
 int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
@@ -340,7 +345,8 @@ int ep_set_option(ep_ctx_t *ctx, int32_t option, int64_t value);
 #define EP_K_ZERO_PAD 6
 #define EP_K_COMBINE_TWO_STAGE 7
 #define EP_K_DISPATCH_FUSED 8   /* routing + fused row movement in one launch */
-#define EP_K_COUNT 9
+#define EP_K_DISPATCH_SMALL 9   /* the same for a small batch, without waits between CTAs */
+#define EP_K_COUNT 10
 
 typedef struct ep_kernel_times {
     int64_t launches[EP_K_COUNT]; /* kernels launched, per kind, since the last read */

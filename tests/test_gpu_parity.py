@@ -249,6 +249,7 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     dispatch on the same context is correct again."""
     x = _custom(2, 8, 2, 1024, 64, seed=3)      # 16 routing tiles per rank
     ctx = H.make_ctx(x, dev)
+    ctx.set_option(L.EP_OPT_SMALL_DISPATCH, 0)   # the tiled routing, whose tiles wait on each other
     ctx.set_option(L.EP_OPT_WAIT_LIMIT_NS, 20_000_000)
     ctx.set_option(L.EP_OPT_FAULT_SKIP_PUBLISH, 2)
     a1, ids, w, nt, extras = H.inputs_dev(x, dev)
@@ -277,18 +278,26 @@ def test_wait_limit_reports_timeout_then_recovers(dev):
     {L.EP_OPT_ROUTE_CTAS: 3, L.EP_OPT_MOVE_PIPES: 4},
     {L.EP_OPT_ROUTE_CTAS: 4096},
     {L.EP_OPT_ROUTE_CTAS: 0},
+    {L.EP_OPT_SMALL_DISPATCH: -1},
+    {L.EP_OPT_SMALL_DISPATCH: 1, L.EP_OPT_KERNEL_TIMING: 1},
+    {L.EP_OPT_SMALL_DISPATCH: 1, L.EP_OPT_PDL: 1},
 ])
 @pytest.mark.parametrize("path", ["fused", "sendbuf"])
 def test_launch_options_do_not_change_results(dev, opts, path):
     x = wl.make(wl.spec(4, T=128))   # 8 KiB rows plus a 128-byte extra payload
-    _roundtrip(x, dev, opts=opts, path=path, ctx_kw=dict(sendbuf=path == "sendbuf"))
+    # a batch this small takes the small-batch dispatch unless it is turned off;
+    # the other options shape the tiled one-launch dispatch
+    _roundtrip(x, dev, opts={L.EP_OPT_SMALL_DISPATCH: 0, **opts}, path=path,
+               ctx_kw=dict(sendbuf=path == "sendbuf"))
 
 
-# 32 routing tiles (every CTA routes) and 96 (32 elected routers)
-@pytest.mark.parametrize("T", [64, 160])
-def test_repeated_steps_are_identical(dev, T):
+# 32 routing tiles (every CTA routes) and 96 (32 elected routers); at T = 64 also
+# the small-batch dispatch
+@pytest.mark.parametrize("T,small", [(64, 0), (64, -1), (160, -1)])
+def test_repeated_steps_are_identical(dev, T, small):
     x = wl.make(wl.spec(5, T=T))
     ctx = H.make_ctx(x, dev)
+    ctx.set_option(L.EP_OPT_SMALL_DISPATCH, small)
     a1, ids, w, nt, extras = H.inputs_dev(x, dev)
     outs = []
     for _ in range(4):
