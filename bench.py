@@ -794,7 +794,10 @@ def run_ours(args):
                           f"(step {sum(step_ms_ev) / n:.4f} ms with those events)",
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     **({"traffic_source": "profiles/dram_traffic.txt (one-launch ncu capture; "
+                                           "rows still dirty in L2 at the kernel's end are not "
+                                           "counted)"} if traffic is not None else {})},
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
