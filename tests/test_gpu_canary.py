@@ -12,6 +12,7 @@ import pytest
 import torch
 
 from combine_ep_route_gb300 import (AgrsBuffers, DispatchOut, EpConfig, EpContext, agrs, workloads as wl)
+from combine_ep_route_gb300 import _lib as L
 from combine_ep_route_gb300 import ep as E
 from oracle import ref
 from tests import _gpu_harness as H
@@ -70,15 +71,19 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
-@pytest.mark.parametrize("path", ["fused", "sendbuf"])
-def test_no_writes_outside_any_buffer(dev, case, path):
+@pytest.mark.parametrize("variant", ["fused", "fused_tiled", "sendbuf"])
+def test_no_writes_outside_any_buffer(dev, case, variant):
+    """These batches are small: "fused" takes the small-batch dispatch,
+    "fused_tiled" the tiled one-launch dispatch."""
     s, nt = CASES[case]
+    path = "sendbuf" if variant == "sendbuf" else "fused"
     x = wl.make(s, num_tokens=nt)
     g = Guarded(dev)
     cfg = EpConfig(s.W, s.E, s.K, s.T, s.h, extra_row_bytes=tuple(x.extra_row_bytes),
                    sendbuf=path == "sendbuf", zero_pad=True)
     ws = g.tensor((E.workspace_bytes(cfg),), torch.uint8)
     ctx = EpContext(cfg, dev, workspace=ws)
+    ctx.set_option(L.EP_OPT_SMALL_DISPATCH, 0 if variant == "fused_tiled" else -1)
     a1, ids, w, ntd, extras = H.inputs_dev(x, dev)
     out = _dispatch_outputs(g, ctx, x)
     ctx.dispatch(a1, ids, w, num_tokens=ntd, extras=extras, out=out, path=path)

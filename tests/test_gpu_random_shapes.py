@@ -2,16 +2,18 @@
 
 Each case draws W, E (a multiple of W), top_k (not always a power of two),
 max_tokens (rarely a multiple of the 64-token routing tile), the hidden size,
-extra payloads, padding rows, a ragged num_tokens, the dispatch path and the
-output type, then checks dispatch (metadata and every delivered row, bit for
-bit) and combine (bit for bit) against the CPU oracle, and the all-gather /
-reduce-scatter route on the same inputs.
+extra payloads, padding rows, a ragged num_tokens, the dispatch path, whether a
+small batch may take the small-batch dispatch, and the output type, then checks
+dispatch (metadata and every delivered row, bit for bit) and combine (bit for
+bit) against the CPU oracle, and the all-gather / reduce-scatter route on the
+same inputs.
 """
 import numpy as np
 import pytest
 import torch
 
 from combine_ep_route_gb300 import agrs, EpConfig, workloads as wl
+from combine_ep_route_gb300 import _lib as L
 from oracle import ref
 from tests import _gpu_harness as H
 
@@ -37,7 +39,8 @@ def _case(i: int):
         nt = rng.integers(0, T + 1, size=W).astype(np.int32)
     path = "sendbuf" if rng.random() < 0.4 else "fused"
     out_f32 = bool(rng.random() < 0.3)
-    return spec, nt, path, out_f32
+    small = -1 if rng.random() < 0.5 else 0   # small-batch dispatch allowed, or the tiled one
+    return spec, nt, path, out_f32, small
 
 
 @pytest.fixture(scope="module")
@@ -51,10 +54,11 @@ def dev():
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_shape(dev, i):
-    spec, nt, path, out_f32 = _case(i)
+    spec, nt, path, out_f32, small = _case(i)
     x = wl.make(spec, num_tokens=nt)
     s = x.spec
     ctx = H.make_ctx(x, dev, sendbuf=path == "sendbuf")
+    ctx.set_option(L.EP_OPT_SMALL_DISPATCH, small)
     a1, ids, w, ntd, extras = H.inputs_dev(x, dev)
     out = ctx.dispatch(a1, ids, w, num_tokens=ntd, extras=extras, path=path)
     ctx.check()
