@@ -66,6 +66,8 @@ def test_named_small_workloads(dev, cfg):
     (4, 8, 8, 40, 256, 0.0, ()),           # top_k > e_local: two slots per token
     (1, 6, 3, 50, 64, 0.1, ()),            # one rank: a counting sort by expert
     (8, 64, 8, 128, 5120, 0.05, (16,)),    # 10 KiB rows with an extra payload
+    (4, 8, 1, 100, 64, 0.1, ()),           # top_k 1
+    (8, 8, 5, 60, 64, 0.0, (4,)),          # one expert per rank, top_k 5 (not a power of two)
 ])
 def test_small_edge_shapes_match_oracle_and_tiled_path(dev, W, E, K, T, h, pad, extras):
     x = _custom(W, E, K, T, h, seed=W * 7 + T, pad=pad, extras=extras)
