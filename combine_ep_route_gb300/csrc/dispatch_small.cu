@@ -38,6 +38,8 @@ namespace {
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallIdBatch = 4;   // earlier tokens whose ids a thread loads together
+static_assert(kSmallThreads >= EP_MAX_W, "one thread per rank loads the token counts");
+static_assert(kSmallMaxTokens <= 32, "an own token is one bit of a 32-bit lane mask");
 
 // Top-k ids of flat token g into ek (-1 past K); g < 0 gives all -1.
 template <int KT>
