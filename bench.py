@@ -229,7 +229,7 @@ class ClockSampler:
 
 class NvmlSampler:
     """SM clock, power and clock-event (throttle) reasons read through NVML's
-    read-only queries every ~1 ms on a background thread, so that even a timed
+    read-only queries every ~0.5 ms on a background thread, so that even a timed
     region of a few milliseconds holds several samples. ``mark()`` opens and
     closes named windows (the timed passes); ``summary(name)`` describes the
     samples inside one. Nothing here changes any GPU setting. Falls back to
@@ -238,7 +238,7 @@ class NvmlSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, cuda_index: int, interval_s: float = 0.001):
+    def __init__(self, cuda_index: int, interval_s: float = 0.0005):
         import ctypes
         import threading
         self.ok = False
@@ -316,7 +316,7 @@ class NvmlSampler:
                 "sm_mhz_min": min(sm) if sm else None,
                 "power_w_max": max(pw) if pw else None,
                 "window_ms": (t1 - t0) * 1e3 if t0 is not None and t1 is not None else None,
-                "source": "NVML read-only queries every ~1 ms on a host thread"}
+                "source": "NVML read-only queries every ~0.5 ms on a host thread"}
 
 
 def replica_aggregate(ms_local: float, tokens_local: int, dist=None, device=None):
