@@ -350,7 +350,7 @@ int auto_route_ctas(const ep_ctx *c) {
 // read (W * max_tokens * top_k <= kSmallMaxIds), one CTA per SM must cover the
 // slots with at most kSmallMaxTokens each, and their rows must fit in shared
 // memory. Needs num_sms (set on first use).
-int small_n_per(const ep_ctx *c, uint32_t *stage_bytes, size_t *smem) {
+int small_n_per(const ep_ctx *c, uint32_t *stage_bytes, size_t *smem, int *threads) {
     if (c->small_dispatch == 0 || c->num_sms < 1) return 0;
     const ep_config_t &cf = c->cfg;
     const long long slots = (long long)cf.W * cf.max_tokens;
@@ -358,10 +358,17 @@ int small_n_per(const ep_ctx *c, uint32_t *stage_bytes, size_t *smem) {
     const long long n_per = (slots + c->num_sms - 1) / c->num_sms;
     if (n_per > ep::kSmallMaxTokens) return 0;
     const uint32_t sb = (uint32_t)align_up(c->L.row_bytes, 128);
-    const size_t bytes = ep::small_smem_bytes((int)n_per, sb, c->L.n_ctr, cf.top_k, cf.W);
+    // the most threads whose warp-private counters still fit
+    int nt = ep::small_threads(cf.top_k);
+    size_t bytes = ep::small_smem_bytes((int)n_per, sb, c->L.n_ctr, cf.top_k, cf.W, nt);
+    while (bytes > ep::kMoveSmemBudget && nt > 256) {
+        nt /= 2;
+        bytes = ep::small_smem_bytes((int)n_per, sb, c->L.n_ctr, cf.top_k, cf.W, nt);
+    }
     if (bytes > ep::kMoveSmemBudget) return 0;
     *stage_bytes = sb;
     *smem = bytes;
+    *threads = nt;
     return (int)n_per;
 }
 
@@ -616,7 +623,8 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
     }
     uint32_t small_sb = 0;
     size_t small_smem = 0;
-    const int small = one_launch ? small_n_per(ctx, &small_sb, &small_smem) : 0;
+    int small_nt = 0;
+    const int small = one_launch ? small_n_per(ctx, &small_sb, &small_smem, &small_nt) : 0;
     if (small > 0) {
         ep::SmallParams sp;
         std::memset(&sp, 0, sizeof(sp));
@@ -635,7 +643,8 @@ int ep_dispatch(ep_ctx_t *ctx, const void *a1, const int32_t *num_tokens, const 
         const int slots = cf.W * cf.max_tokens;
         const int grid = (slots + small - 1) / small;
         KernelTimer tm(ctx, EP_K_DISPATCH_SMALL, st);
-        if (ep::launch_dispatch_small(sp, grid, small_smem, st) != cudaSuccess) return EP_ERR_CUDA;
+        if (ep::launch_dispatch_small(sp, grid, small_nt, small_smem, st) != cudaSuccess)
+            return EP_ERR_CUDA;
     } else if (one_launch) {
         fm.wait_tiles = 1;
         fm.dynamic_units = 1;

@@ -35,10 +35,11 @@ namespace ep {
 
 namespace {
 
-constexpr int kSmallThreads = 256;
-constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallIdBatch = 4;   // earlier tokens whose ids a thread loads together
-static_assert(kSmallThreads >= EP_MAX_W, "one thread per rank loads the token counts");
+// A CTA has NT threads (256, 512 or 1024: more threads share the prefix count);
+// each loads the ids of 1024 / NT earlier tokens per round.
+constexpr int kSmallMinThreads = 256;
+constexpr int kSmallRoundTokens = 1024;   // earlier tokens whose ids a CTA loads per round
+static_assert(kSmallMinThreads >= EP_MAX_W, "one thread per rank loads the token counts");
 static_assert(kSmallMaxTokens <= 32, "an own token is one bit of a 32-bit lane mask");
 
 // Top-k ids of flat token g into ek (-1 past K); g < 0 gives all -1.
@@ -80,14 +81,17 @@ __device__ __forceinline__ uint32_t kept_pairs(const int (&ek)[KT], int K, int E
 // [warps][W+E], the prefix [W+E], the own-token masks [W+E], the own pairs
 // [32][KT] (packed destination and expert) with their weights, and the
 // clamped token counts [W].
-size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W) {
+size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W, int threads) {
     const size_t rows = ((size_t)n_per * stage_bytes + 127) / 128 * 128;
-    return rows + 16 + (size_t)(kSmallWarps + 2) * n_ctr * 4 +
+    return rows + 16 + (size_t)(threads / 32 + 2) * n_ctr * 4 +
            (size_t)kSmallMaxTokens * route_kt(top_k) * 8 + (size_t)W * 4;
 }
 
-template <int KT>
-__global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(const SmallParams sp) {
+template <int KT, int NT>
+__global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp) {
+    constexpr int kSmallThreads = NT;
+    constexpr int kSmallWarps = NT / 32;
+    constexpr int kSmallIdBatch = kSmallRoundTokens / NT;
     extern __shared__ __align__(128) uint8_t smem[];
     const RouteParams &p = sp.rp;
     const MoveParams &m = sp.mp;
@@ -365,20 +369,39 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(const Sma
     if (tid == 0 && !waited) mbar_wait_bounded(bar, 0u, p.wait_limit_ns, p.hdr);
 }
 
-cudaError_t launch_dispatch_small(const SmallParams &sp, int grid, size_t smem, cudaStream_t st) {
-    const void *fn = nullptr;
-    switch (route_kt(sp.rp.K)) {
-        case 1: fn = (const void *)dispatch_small_kernel<1>; break;
-        case 2: fn = (const void *)dispatch_small_kernel<2>; break;
-        case 4: fn = (const void *)dispatch_small_kernel<4>; break;
-        case 8: fn = (const void *)dispatch_small_kernel<8>; break;
-        case 16: fn = (const void *)dispatch_small_kernel<16>; break;
-        default: return cudaErrorInvalidValue;
+template <int KT, int NT>
+static const void *small_kernel() {
+    if constexpr (KT == 16 && NT > 512) return nullptr;   // registers: see small_threads
+    else return (const void *)dispatch_small_kernel<KT, NT>;
+}
+
+template <int NT>
+static const void *small_fn(int top_k) {
+    switch (route_kt(top_k)) {
+        case 1: return small_kernel<1, NT>();
+        case 2: return small_kernel<2, NT>();
+        case 4: return small_kernel<4, NT>();
+        case 8: return small_kernel<8, NT>();
+        case 16: return small_kernel<16, NT>();
+        default: return nullptr;
     }
+}
+
+// Threads per CTA of the small-batch dispatch: as many as the registers of one
+// CTA per SM allow (the kernel for top_k 16 needs more registers per thread).
+int small_threads(int top_k) { return route_kt(top_k) <= 8 ? 1024 : 512; }
+
+cudaError_t launch_dispatch_small(const SmallParams &sp, int grid, int threads, size_t smem,
+                                  cudaStream_t st) {
+    const void *fn = threads == 1024 ? small_fn<1024>(sp.rp.K)
+                   : threads == 512  ? small_fn<512>(sp.rp.K)
+                   : threads == 256  ? small_fn<256>(sp.rp.K)
+                                     : nullptr;
+    if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = ensure_dyn_smem(fn, smem);
     if (e != cudaSuccess) return e;
     void *args[] = {const_cast<SmallParams *>(&sp)};
-    e = cudaLaunchKernel(fn, dim3(grid), dim3(kSmallThreads), args, smem, st);
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, smem, st);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

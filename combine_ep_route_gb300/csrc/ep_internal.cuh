@@ -350,8 +350,10 @@ cudaError_t launch_move(int mode, const MoveParams &p, int grid, int block, size
 // Routing and the fused row movement in one persistent launch (grid = resident CTAs).
 cudaError_t launch_dispatch_fused(const RouteParams &rp, const MoveParams &mp, int grid,
                                   size_t move_smem, cudaStream_t st);
-size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W);
-cudaError_t launch_dispatch_small(const SmallParams &sp, int grid, size_t smem, cudaStream_t st);
+size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W, int threads);
+int small_threads(int top_k);
+cudaError_t launch_dispatch_small(const SmallParams &sp, int grid, int threads, size_t smem,
+                                  cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, bool out_f32, int grid, bool pdl,
                            cudaStream_t st);
 cudaError_t combine_occupancy(int top_k, bool out_f32, int *ctas_per_sm);
