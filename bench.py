@@ -70,6 +70,8 @@ def parse():
                     help="tokens per rank drawn uniformly in [T/2, T] (seeded)")
     ap.add_argument("--zero-pad", action="store_true",
                     help="also zero every batched-expert row past the expert's count, as the page does")
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"],
+                    help="combine output type (f32: the fp32-output variant; an auxiliary line)")
     ap.add_argument("--hot", action="store_true",
                     help="no L2 flush between timed steps: the L2-resident figure of a small "
                          "workload, reported beside the flushed one, never as the headline")
@@ -360,6 +362,8 @@ def variant_of(args) -> dict:
         v["ragged"] = "num_tokens ~ U[T/2, T] per rank, seed 7"
     if args.zero_pad:
         v["zero_pad"] = True
+    if getattr(args, "out_dtype", "bf16") != "bf16":
+        v["out_dtype"] = args.out_dtype
     if getattr(args, "option", None):
         v["options"] = sorted(args.option)
     return v
@@ -640,11 +644,15 @@ def run_ours(args):
     # identity experts read the dispatched rows; quantised rows need a bf16 expert output
     expert_out = out.b_a1 if not quant else torch.zeros(
         (s.W, s.E // s.W, ctx.expert_cap, s.h), dtype=torch.bfloat16, device=dev)
-    y = torch.empty((s.W, s.T, s.h), dtype=torch.bfloat16, device=dev)
+    out_t = torch.float32 if args.out_dtype == "f32" else torch.bfloat16
+    y = torch.empty((s.W, s.T, s.h), dtype=out_t, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    combine = ctx.combine if args.combine == "fused" else ctx.combine_two_stage
+    combine_fn = ctx.combine if args.combine == "fused" else ctx.combine_two_stage
+
+    def combine(eo, out):
+        return combine_fn(eo, out=out, out_dtype=out_t)
 
     def step():
         ctx.dispatch(a1, ids, w, num_tokens=nt, extras=extras, out=out, path=args.path)
@@ -743,7 +751,8 @@ def run_ours(args):
         clocks["other_passes"] = {k: nv.summary(k) for k in ("per_kernel", "separate_calls")}
     med_d = float(np.median([e[0].elapsed_time(e[1]) for e in evm]))
     med_c = float(np.median([e[1].elapsed_time(e[2]) for e in evm]))
-    disp_b, comb_b = algorithmic_bytes(x, x_row_bytes=cfg.x_row_bytes, extra_bytes=sum(extra_row_bytes))
+    disp_b, comb_b = algorithmic_bytes(x, out_bytes_per_elem=4 if args.out_dtype == "f32" else 2,
+                                       x_row_bytes=cfg.x_row_bytes, extra_bytes=sum(extra_row_bytes))
     n_pairs, n_tok_routed, n_tok = workload_counts(x)
     ms, _, value = replica_aggregate(sum(step_ms) / n, n_tok, dist if world > 1 else None, dev)
     peak, peak_src = measured_peaks()
@@ -780,7 +789,7 @@ def run_ours(args):
         "config": {"workload": s.name, "W": s.W, "E": s.E, "top_k": s.K, "tokens_per_rank": s.T,
                    "hidden": s.h, "extra_row_bytes": list(extra_row_bytes), "path": args.path,
                    "combine": args.combine, "launch": "cuda graph replay" if args.graph else "stream",
-                   "out_dtype": "bf16", "accumulate": "f32",
+                   "out_dtype": args.out_dtype, "accumulate": "f32",
                    "experts": ("identity (expert_out = b_a1)" if not quant else
                                "a bf16 expert-output buffer (the dispatched rows are quantised)"),
                    "l2": ("hot: no flush between steps" if args.hot else
