@@ -1032,6 +1032,29 @@ def run_ceilings(args):
            "write_only": timed(lambda: b.zero_(), n),
            "copy": timed(lambda: b.copy_(a), 2 * n)}
     del a, b
+    # the fixed cost a timed step carries: a replayed graph of one or two minimal
+    # kernels between the step's events, after the 256 MiB L2-flushing write
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tiny = [torch.zeros(16, dtype=torch.int32, device=dev) for _ in range(2)]
+    floor = {}
+    for n_k in (1, 2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(n_k):
+                tiny[k].zero_()
+        us = []
+        for i in range(220):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            g.replay()
+            e1.record(st)
+            e1.synchronize()
+            if i >= 20:
+                us.append(e0.elapsed_time(e1) * 1e3)
+        floor[f"{n_k}_kernel_graph_us"] = {"median": float(np.median(us)), "min": float(min(us))}
+    out["launch_floor"] = floor
+    del flush
     m = 118 << 20
     h_src = torch.ones(m, dtype=torch.uint8).pin_memory()
     h_dst = torch.empty(m, dtype=torch.uint8).pin_memory()
@@ -1053,7 +1076,9 @@ def run_ceilings(args):
     out["note"] = ("read_only: the fastest of four torch reductions over 1 GiB (a lower bound on "
                    "the read ceiling); write_only: zero_ of 1 GiB; copy: copy_ of "
                    "1 GiB (read + write bytes); host link: cudaMemcpyAsync through torch on "
-                   "pinned 118 MiB buffers, both directions on two streams at once")
+                   "pinned 118 MiB buffers, both directions on two streams at once; launch_floor: "
+                   "a replayed CUDA graph of one or two 64-byte zero_ kernels between CUDA events, "
+                   "after the L2 flush, as the timed steps are (200 repetitions)")
     if rank == 0:
         print(json.dumps(out), flush=True)
 
