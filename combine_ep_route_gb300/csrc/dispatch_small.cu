@@ -22,10 +22,11 @@
 //   2. one thread per own token validates its ids and sets its lane bit in
 //      per-expert and per-destination masks (a token reaching a rank twice sets
 //      one bit: the (destination, token) deduplication);
-//   3. one thread per own (token, k) pair derives the pair's row and slot from
-//      the prefix and the masks, writes the pair outputs, and stores the row to
-//      its expert's batch with a bulk copy from shared memory; the first pair of
-//      a token on a destination writes that destination's received-slot row;
+//   3. every own (token, k) pair derives its row and slot from the prefix and
+//      the masks twice, in two warps' threads: one stores the row to its expert's
+//      batch with a bulk copy from shared memory, the other writes the pair
+//      outputs and, for the first pair of a token on a destination, that
+//      destination's received-slot row;
 //   4. the CTA holding a rank's last token slot writes that rank's send counts,
 //      and the one holding the very last slot writes expert_num_tokens.
 // The only wait is the bounded one on the row copies' mbarrier.
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
     }
     __syncthreads();
 
-    // 3. one thread per own (token, k) pair
+    // 3. the own (token, k) pairs: row copies and metadata
     auto rank_mask = [&](int s) -> uint32_t {   // own tokens of rank s
         const int lo = max(s * Tm - g0, 0), hi = min((s + 1) * Tm - g0, n_own);
         if (hi <= lo) return 0u;
@@ -259,24 +260,31 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
             if (k2 < k && te[k2] >= 0 && (te[k2] >> 16) == d) first = false;
         return first;
     };
+    // Each pair has two jobs, held by threads of different warps: the first n_pad
+    // threads store the rows (bulk copies from shared memory), the next n_pad write
+    // the pair outputs and received-slot rows. A warp's bulk-copy instruction
+    // completes only once the copy engine has taken all its lanes' copies (~3.5 us
+    // for 32 rows of 4 KiB), so metadata stores issued by the same threads after it
+    // would finish only then.
+    const int n_pairs = n_own * KT;
+    const int n_pad = (n_pairs + 31) & ~31;
     bool waited = false, loaded = false, stored = false;
-    for (int pi = tid; pi < n_own * KT; pi += kSmallThreads) {
+    for (int wi = tid; wi < 2 * n_pad; wi += kSmallThreads) {
+        const bool meta = wi >= n_pad;
+        const int pi = meta ? wi - n_pad : wi;
+        if (pi >= n_pairs) continue;
         const int tl = pi / KT, k = pi - (pi / KT) * KT;
         if (k >= K) continue;
         const int g = g0 + tl;
         const int s = (int)fastdiv((uint32_t)g, sp.div_tm);
         const int32_t *te = sid + tl * KT;
         const int pk = te[k];
-        int32_t prow = -1, psend = -1;
-        float pw = 0.f;
         int slot = 0, row = 0;
-        if (locate(tl, pk, slot, row)) {
-            const int e = pk & 0xFFFF, d = pk >> 16;
-            prow = e * p.Ecap + row;
-            pw = p.unit_weights ? 1.0f : sw[tl * KT + k];
-            const bool first = first_on_dest(te, k, d);
-            if (first) psend = (s * W + d) * Tm + slot;
+        const bool found = locate(tl, pk, slot, row);
+        if (!meta) {
             // the row, from shared memory to the pair's row of its expert
+            if (!found) continue;
+            const int prow = (pk & 0xFFFF) * p.Ecap + row;
             if (!waited) {
                 loaded = mbar_wait_bounded(bar, 0u, p.wait_limit_ns, p.hdr);
                 waited = true;
@@ -288,6 +296,16 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
                              m.seg_bytes[sg]);
                 stored = true;
             }
+            continue;
+        }
+        int32_t prow = -1, psend = -1;
+        float pw = 0.f;
+        if (found) {
+            const int e = pk & 0xFFFF, d = pk >> 16;
+            prow = e * p.Ecap + row;
+            pw = p.unit_weights ? 1.0f : sw[tl * KT + k];
+            const bool first = first_on_dest(te, k, d);
+            if (first) psend = (s * W + d) * Tm + slot;
             if (first) {
                 // the received-slot row on d: the token's pairs on d in top-k order
                 const uint32_t lt = (1u << tl) - 1u;
