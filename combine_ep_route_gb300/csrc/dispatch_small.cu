@@ -80,12 +80,12 @@ __device__ __forceinline__ uint32_t kept_pairs(const int (&ek)[KT], int K, int E
 
 // Shared memory: the CTA's rows, an mbarrier, warp-private counters
 // [warps][W+E], the prefix [W+E], the own-token masks [W+E], the own pairs
-// [32][KT] (packed destination and expert) with their weights, and the
-// clamped token counts [W].
+// [32][KT] (packed destination and expert) with their weights, the clamped
+// token counts [W], and the own tokens' ids as read [32][KT].
 size_t small_smem_bytes(int n_per, uint32_t stage_bytes, int n_ctr, int top_k, int W, int threads) {
     const size_t rows = ((size_t)n_per * stage_bytes + 127) / 128 * 128;
     return rows + 16 + (size_t)(threads / 32 + 2) * n_ctr * 4 +
-           (size_t)kSmallMaxTokens * route_kt(top_k) * 8 + (size_t)W * 4;
+           (size_t)kSmallMaxTokens * route_kt(top_k) * 12 + (size_t)W * 4;
 }
 
 template <int KT, int NT>
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
     int32_t *sid = reinterpret_cast<int32_t *>(bits + n_ctr);      // [32][KT]
     float *sw = reinterpret_cast<float *>(sid + kSmallMaxTokens * KT);   // [32][KT]
     int32_t *sT = reinterpret_cast<int32_t *>(sw + kSmallMaxTokens * KT);   // [W]
+    int32_t *sraw = sT + W;                                                  // [32][KT]
 
     // a combine launched with programmatic dependent launch may start its
     // prologue now; it waits for this grid's completion before reading anything
@@ -131,11 +132,15 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
     }
     int T_in = Tm;
     if (tid < W && p.num_tokens) T_in = __ldg(p.num_tokens + tid);
-    int own_ids[KT];      // the own token's ids (tid < n_own)
-    float wk[KT];
-    load_ids<KT>(p, tid < n_own ? g0 + tid : -1, own_ids);
+    if (tid < n_own) {   // the own token's ids and weights, as read
+        int own_ids[KT];
+        load_ids<KT>(p, g0 + tid, own_ids);
 #pragma unroll
-    for (int k = 0; k < KT; ++k) wk[k] = (tid < n_own && k < K) ? __ldg(p.weights + (size_t)(g0 + tid) * K + k) : 0.f;
+        for (int k = 0; k < KT; ++k) {
+            sraw[tid * KT + k] = own_ids[k];
+            sw[tid * KT + k] = k < K ? __ldg(p.weights + (size_t)(g0 + tid) * K + k) : 0.f;
+        }
+    }
     int ek[kSmallIdBatch][KT];
 #pragma unroll
     for (int b = 0; b < kSmallIdBatch; ++b) {
@@ -190,43 +195,39 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
         }
     }
 
-    // 2. one thread per own token: validate, lane bits per expert and destination
-    if (tid < n_own) {
-        const int g = g0 + tid;
+    // 2. one thread per own (token, k) pair: validate, and set the token's lane
+    // bit for its expert and destination. A valid id repeated at a later k of the
+    // same token is the duplicate (the first occurrence of a valid id is always
+    // kept), and a token that reaches a rank twice sets one bit: the
+    // (destination, token) deduplication.
+    for (int pi = tid; pi < n_own * KT; pi += kSmallThreads) {
+        const int tl = pi / KT, k = pi - (pi / KT) * KT;
+        const int g = g0 + tl;
         const int s = (int)fastdiv((uint32_t)g, sp.div_tm);
-        if (g - s * Tm >= sT[s]) {
-#pragma unroll
-            for (int k = 0; k < KT; ++k) own_ids[k] = -1;
+        const int32_t *raw = sraw + tl * KT;
+        const int e = (k < K && g - s * Tm < sT[s]) ? raw[k] : -1;
+        bool ok = e >= 0;
+        if (ok && e >= E) {
+            raise_error(p.hdr, EP_ERR_EXPERT_ID);
+            ok = false;
         }
-        uint32_t keep = 0;
+        if (ok) {
+            bool dup = false;
 #pragma unroll
-        for (int k = 0; k < KT; ++k) {
-            const int e = own_ids[k];
-            bool ok = k < K && e >= 0;
-            if (ok && e >= E) {
-                raise_error(p.hdr, EP_ERR_EXPERT_ID);
+            for (int k2 = 0; k2 < KT; ++k2) dup |= k2 < k && raw[k2] == e;
+            if (dup) {
+                raise_error(p.hdr, EP_ERR_DUPLICATE);
                 ok = false;
             }
-            if (ok) {
-                bool dup = false;
-#pragma unroll
-                for (int k2 = 0; k2 < k; ++k2) dup |= ((keep >> k2) & 1u) && own_ids[k2] == e;
-                if (dup) {
-                    raise_error(p.hdr, EP_ERR_DUPLICATE);
-                    ok = false;
-                }
-            }
-            int packed = -1;
-            if (ok) {
-                const int d = (int)fastdiv((uint32_t)e, sp.div_el);
-                keep |= 1u << k;
-                atomicOr(&bits[d], 1u << tid);
-                atomicOr(&bits[W + e], 1u << tid);
-                packed = (d << 16) | e;
-            }
-            sid[tid * KT + k] = packed;
-            sw[tid * KT + k] = wk[k];
         }
+        int packed = -1;
+        if (ok) {
+            const int d = (int)fastdiv((uint32_t)e, sp.div_el);
+            atomicOr(&bits[d], 1u << tl);
+            atomicOr(&bits[W + e], 1u << tl);
+            packed = (d << 16) | e;
+        }
+        sid[pi] = packed;
     }
     __syncthreads();
     for (int c = tid; c < n_ctr; c += kSmallThreads) {
