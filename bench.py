@@ -134,14 +134,43 @@ KERNEL_TU = {"dispatch_fused": "move.cu", "dispatch_small": "dispatch_small.cu",
              "agrs_gather": "agrs.cu", "agrs_experts": "agrs.cu", "agrs_reduce": "agrs.cu"}
 
 
+def code_tokens(src: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace runs collapsed to
+    one space (string and character literals kept as written), so that edits
+    to comments or layout leave the kernel's hash unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (not the comments) of a kernel's translation unit, the
+    shared headers and api.cu: the key of the committed DRAM figures."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_ep_route_gb300", "csrc")
     names = sorted(n for n in os.listdir(csrc)
                    if n.endswith(".cuh") or n in (KERNEL_TU[kernel], "api.cu"))
     for n in names:
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, n), encoding="utf-8") as f:
+            h.update(n.encode() + b"\0" + code_tokens(f.read()).encode() + b"\0")
     return h.hexdigest()[:16]
 
 

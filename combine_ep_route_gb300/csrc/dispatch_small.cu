@@ -19,9 +19,10 @@
 //      kept pairs of each expert and -- for earlier tokens of the first token's
 //      rank -- the destinations each reaches (warp-private counters in shared
 //      memory, summed afterwards);
-//   2. one thread per own token validates its ids and sets its lane bit in
-//      per-expert and per-destination masks (a token reaching a rank twice sets
-//      one bit: the (destination, token) deduplication);
+//   2. one thread per own (token, k) pair validates the id (staged in shared
+//      memory at launch) and sets the token's lane bit in per-expert and
+//      per-destination masks (a token reaching a rank twice sets one bit: the
+//      (destination, token) deduplication);
 //   3. every own (token, k) pair derives its row and slot from the prefix and
 //      the masks twice, in two warps' threads: one stores the row to its expert's
 //      batch with a bulk copy from shared memory, the other writes the pair
