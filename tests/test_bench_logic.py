@@ -65,6 +65,15 @@ def test_traffic_lookup_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("agrs_gather") == bench.kernel_source_hash("agrs_reduce")
 
 
+def test_source_key_ignores_comments_and_layout_only():
+    code = 'int f(int a) {\n    return a + 1;  // one more\n}\nconst char *s = "x // y";\n'
+    same = '/* doc */ int f(int a)\n{ return a + 1; }\n// trailing\nconst char *s = "x // y";'
+    assert bench.code_tokens(code) == bench.code_tokens(same)
+    assert bench.code_tokens(code) != bench.code_tokens(code.replace("a + 1", "a + 2"))
+    assert bench.code_tokens(code) != bench.code_tokens(code.replace('"x // y"', '"x /* y"'))
+    assert bench.code_tokens("char c = '\\''; int b; // z") == "char c = '\\''; int b;"
+
+
 def test_traffic_only_for_the_unchanged_named_workload(tmp_path, monkeypatch):
     src = bench.kernel_source_hash("dispatch_fused")
     f = tmp_path / "traffic.txt"
