@@ -384,9 +384,13 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
             p.expert_num_tokens[e] = min(max(excl[W + e] + __popc(bits[W + e] & all), 0), p.Ecap);
     }
 
-    // the row copies must be done before the CTA's shared memory goes away
+    // the row copies must be done before the CTA's shared memory goes away: the
+    // stores this thread issued, and the loads into shared memory, which thread 0
+    // waits for (bounded) unless it has seen them complete -- also after a wait
+    // that ran out, so a CTA never exits with its loads still in flight unless a
+    // second full wait runs out as well
     if (stored) bulk_wait_all();
-    if (tid == 0 && !waited) mbar_wait_bounded(bar, 0u, p.wait_limit_ns, p.hdr);
+    if (tid == 0 && !loaded) mbar_wait_bounded(bar, 0u, p.wait_limit_ns, p.hdr);
 }
 
 template <int KT, int NT>

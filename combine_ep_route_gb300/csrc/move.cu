@@ -363,8 +363,9 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     }
     if (lane == 0) {
         if (!ok) {
-            // drain the loads already issued before leaving (bounded)
-            for (int i = consumed + 1; i < issued; ++i)
+            // drain the loads already issued before leaving (bounded), the one
+            // whose wait ran out included
+            for (int i = consumed; i < issued; ++i)
                 if (!mbar_wait_bounded(&bars[i % NS], (uint32_t)(i / NS) & 1u, p.wait_limit_ns, p.hdr))
                     break;
         }
