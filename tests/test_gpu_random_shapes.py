@@ -19,7 +19,7 @@ from tests import _gpu_harness as H
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 80
 
 
 def _case(i: int):
