@@ -918,7 +918,7 @@ def run_agrs(args):
             step()
     n = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    with ClockSampler(local) as clk:
+    def timed():
         torch.cuda.synchronize()
         for i in range(n):
             flush.zero_()
@@ -926,6 +926,18 @@ def run_agrs(args):
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+
+    nv = NvmlSampler(local)
+    if nv.ok:
+        with nv:
+            nv.mark("timed", True)
+            timed()
+            nv.mark("timed", False)
+        clocks = nv.summary("timed")
+    else:
+        with ClockSampler(local) as clk:
+            timed()
+        clocks = clk.summary()
     if int(buf.status.item()) != 0:
         raise SystemExit(f"device status {int(buf.status.item())} after the timed region")
     ms = sum(a.elapsed_time(b) for a, b in ev) / n
@@ -952,7 +964,7 @@ def run_agrs(args):
                      "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} hbm_gbs",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic},
         "gpu_launches": 3 * n,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
