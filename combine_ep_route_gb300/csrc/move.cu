@@ -197,8 +197,12 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     // tile in the same launch) takes fewer units, while small problems never
     // touch the counter. The last two rounds are grabbed one unit at a time, so
     // the warps finish within about one unit of each other. Called with i
-    // growing by at most one per new value.
-    constexpr int kStaticUnits = 2, kUnitBatch = 4;
+    // growing by at most one per new value. One static unit per warp, batches of
+    // four and two single-unit rounds measured best on GB300 (prefill dispatch
+    // 173.4 -> 172.9 us, Zipf 109.6 -> 109.1, grouped 150.9 -> 150.5; two static
+    // units, batches of 2, 3, 6 or 8 and one, three or four final rounds were
+    // slower).
+    constexpr int kStaticUnits = 1, kUnitBatch = 4;
     const bool dyn = p.dynamic_units != 0;
     const int tail_from = n_work - 2 * kUnitBatch * stride;
     int seq_base = 0, seq_len = 0, seq_i0 = kStaticUnits;
