@@ -11,10 +11,10 @@
 // all earlier tokens (read through L2) instead of waiting on a chain of
 // look-back flags published by other CTAs. A CTA owns at most 32 consecutive
 // token slots:
-//   0. every global read is issued at launch: thread 0 starts bulk copies of the
-//      CTA's token rows (and extra payloads) into shared memory, and the threads
-//      load the token counts, the own tokens' ids and weights and the first
-//      batch of earlier tokens' ids, so the whole kernel waits on one round trip;
+//   0. the threads load the token counts, the own tokens' ids and weights and
+//      the first batch of earlier tokens' ids at launch; after the first barrier
+//      thread 0 starts bulk copies of the CTA's token rows (and extra payloads)
+//      into shared memory, which arrive while the prefix is counted;
 //   1. every thread counts, over a strided share of the earlier tokens, the
 //      kept pairs of each expert and -- for earlier tokens of the first token's
 //      rank -- the destinations each reaches (warp-private counters in shared
@@ -119,17 +119,12 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
     // prologue now; it waits for this grid's completion before reading anything
     pdl_launch_dependents();
 
-    // 0. every global read starts at once: the CTA's rows (bulk copies into
-    // shared memory), the token counts, the own tokens' ids and weights, and the
-    // first batch of earlier tokens' ids
+    // 0. every small global read starts at once: the token counts, the own
+    // tokens' ids and weights, and the first batch of earlier tokens' ids; the
+    // CTA's rows follow right after the first barrier (below)
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar, (uint32_t)n_own * m.row_bytes);
-        for (int i = 0; i < n_own; ++i)
-            for (int sg = 0; sg < m.n_seg; ++sg)
-                bulk_g2s(rows + (size_t)i * sb + m.seg_off[sg],
-                         m.src_seg[sg] + (size_t)(g0 + i) * m.seg_bytes[sg], m.seg_bytes[sg], bar);
     }
     int T_in = Tm;
     if (tid < W && p.num_tokens) T_in = __ldg(p.num_tokens + tid);
@@ -160,6 +155,16 @@ __global__ void __launch_bounds__(NT) dispatch_small_kernel(const SmallParams sp
         sT[tid] = T;
     }
     __syncthreads();
+    // The rows (bulk copies into shared memory) are needed only once the prefix
+    // is counted; issued at launch they delayed the ids' round trip that the
+    // count waits on (decode step 21.3 -> 20.7 us on GB300 when issued here).
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)n_own * m.row_bytes);
+        for (int i = 0; i < n_own; ++i)
+            for (int sg = 0; sg < m.n_seg; ++sg)
+                bulk_g2s(rows + (size_t)i * sb + m.seg_off[sg],
+                         m.src_seg[sg] + (size_t)(g0 + i) * m.seg_bytes[sg], m.seg_bytes[sg], bar);
+    }
 
     // 1. the prefix of the first own token, counted from the earlier tokens' ids
     const int s0 = (int)fastdiv((uint32_t)g0, sp.div_tm);
