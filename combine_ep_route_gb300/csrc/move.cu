@@ -206,6 +206,8 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     // 173.4 -> 172.9 us, Zipf 109.6 -> 109.1, grouped 150.9 -> 150.5; two static
     // units, batches of 2, 3, 6 or 8 and one, three or four final rounds were
     // slower).
+    // (kStaticUnits must stay at least 1: the fills below read unit_at(0) once
+    // before they take their units, which must not consume a dynamic batch.)
     constexpr int kStaticUnits = 1, kUnitBatch = 4;
     const bool dyn = p.dynamic_units != 0;
     const int tail_from = n_work - 2 * kUnitBatch * stride;
