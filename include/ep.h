@@ -314,7 +314,9 @@ const char *ep_error_string(int code);
                                        publishes, so its successors' waits run out and
                                        report EP_ERR_TIMEOUT; -1 (default) = off */
 #define EP_OPT_COMBINE_CTAS_PER_SM 7 /* combine CTAs per SM (default 0: for top_k above 4 one wave
-                                        of at most 3 per SM; for top_k up to 4 a grid of 16 per SM) */
+                                        of at most 3 per SM, or of all that fit when a wave covers
+                                        the work in at most 4 rounds; for top_k up to 4 a grid of
+                                        16 per SM) */
 #define EP_OPT_MOVE_CHUNK_BYTES 8 /* row-mover unit: rows split into chunks of at least this
                                      many bytes (multiple of 16; 0 = whole rows; -1 = default,
                                      chosen per problem) */
