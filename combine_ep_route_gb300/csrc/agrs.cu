@@ -237,19 +237,20 @@ __global__ void __launch_bounds__(kThreads) agrs_reduce_kernel(const AgrsParams 
                 }
             }
         }
+        // the output is written once and read by nothing here: streaming stores
         if (OUT_F32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
                                                    (size_t)v * 8);
-            o[0] = make_float4(a[0], a[1], a[2], a[3]);
-            o[1] = make_float4(a[4], a[5], a[6], a[7]);
+            __stcs(o, make_float4(a[0], a[1], a[2], a[3]));
+            __stcs(o + 1, make_float4(a[4], a[5], a[6], a[7]));
         } else {
             uint4 o;
             o.x = pack_bf16x2(a[0], a[1]);
             o.y = pack_bf16x2(a[2], a[3]);
             o.z = pack_bf16x2(a[4], a[5]);
             o.w = pack_bf16x2(a[6], a[7]);
-            *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
-                                       (size_t)v * 16) = o;
+            __stcs(reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
+                                             (size_t)v * 16), o);
         }
     }
 }

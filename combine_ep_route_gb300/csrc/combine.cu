@@ -112,19 +112,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
                 fold2(a[4], a[5], w[k], x[k][j].z);
                 fold2(a[6], a[7], w[k], x[k][j].w);
             }
+            // the output is written once and read by nothing here: streaming
+            // (evict-first) stores (measured on GB300: prefill combine 163.6 ->
+            // 162.0 us, Zipf 96.3 -> 93.2, grouped 145.2 -> 142.9, decode unchanged;
+            // an evict-first policy on the row loads instead changed nothing)
             if (OUT_F32) {
                 float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
                                                        (size_t)v * 8);
-                o[0] = make_float4(a[0], a[1], a[2], a[3]);
-                o[1] = make_float4(a[4], a[5], a[6], a[7]);
+                __stcs(o, make_float4(a[0], a[1], a[2], a[3]));
+                __stcs(o + 1, make_float4(a[4], a[5], a[6], a[7]));
             } else {
                 uint4 o;
                 o.x = pack_bf16x2(a[0], a[1]);
                 o.y = pack_bf16x2(a[2], a[3]);
                 o.z = pack_bf16x2(a[4], a[5]);
                 o.w = pack_bf16x2(a[6], a[7]);
-                *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
-                                           (size_t)v * 16) = o;
+                __stcs(reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * row_bytes +
+                                                 (size_t)v * 16), o);
             }
         }
     }
@@ -373,8 +377,8 @@ __global__ void __launch_bounds__(256) combine_gather_kernel(const GatherParams 
             }
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)g * p.h +
                                                    (size_t)v * 8);
-            o[0] = make_float4(a[0], a[1], a[2], a[3]);
-            o[1] = make_float4(a[4], a[5], a[6], a[7]);
+            __stcs(o, make_float4(a[0], a[1], a[2], a[3]));   // streaming, as in combine_kernel
+            __stcs(o + 1, make_float4(a[4], a[5], a[6], a[7]));
         } else {
             // bf16 sums, each rounded, in ascending rank order: native bf16 adds
             // (see add_bf16x2), starting from +0 like the fp32 form
@@ -387,8 +391,8 @@ __global__ void __launch_bounds__(256) combine_gather_kernel(const GatherParams 
                 o.z = add_bf16x2(o.z, x[k].z);
                 o.w = add_bf16x2(o.w, x[k].w);
             }
-            *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
-                                       (size_t)v * 16) = o;
+            __stcs(reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)g * p.h * 2 +
+                                             (size_t)v * 16), o);
         }
     }
 }
@@ -447,9 +451,11 @@ __global__ void __launch_bounds__(256) zero_pad_kernel(const ZeroPadParams p) {
         const size_t bytes = p.seg_bytes[sg];
         uint4 *base = reinterpret_cast<uint4 *>(p.dst_seg[sg] + ((size_t)e * p.Ecap + n) * bytes);
         const size_t nv = (size_t)(p.Ecap - n) * bytes / 16;
+        // streaming stores: the zeros are not read back by this step (measured on
+        // GB300: zero-filled prefill step 4371 -> 4317 us)
         for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
              i += (size_t)gridDim.x * blockDim.x)
-            base[i] = make_uint4(0u, 0u, 0u, 0u);
+            __stcs(base + i, make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
