@@ -26,6 +26,27 @@ namespace ep {
 
 namespace {
 
+// An L2 evict-first policy for the mover's source reads. Every source row (or
+// chunk of one) is read once, so it need not stay in L2, where it would displace
+// the destination rows the combine reads next (measured on GB300: prefill step
+// -0.5 us, Zipf -0.8 us, grouped -0.7 us; the same hint on the stores instead
+// made the combine 2.5-5 us slower).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// global -> shared bulk copy (completion on an mbarrier) with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s_hint(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // Wait (bounded) until a routing tile of this launch has published its
 // outputs. False after the limit (EP_ERR_TIMEOUT raised).
 __device__ __forceinline__ bool wait_tile_done(const uint32_t *f, uint32_t epoch, uint64_t limit_ns,
@@ -130,6 +151,7 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
     constexpr int kStash = kMaxDst + 3;   // per stage: src, count, destinations, chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int P = p.pipes;
+    const uint64_t pol = evict_first_policy();   // source reads
     const int NS = p.stages;
     const size_t stage_region = (size_t)P * NS * p.stage_bytes;
     uint8_t *stages = smem + (size_t)warp * NS * p.stage_bytes;
@@ -244,15 +266,15 @@ __device__ __forceinline__ void move_body(const MoveParams &p, uint8_t *smem, ui
         uint8_t *stg = stages + (size_t)st * p.stage_bytes;
         mbar_arrive_expect_tx(bar, cb + (c == 0 ? tail : 0u));
         if (src_split) {
-            bulk_g2s(stg, p.src_seg[0] + (size_t)src * a1b + (size_t)c * cb, cb, bar);
+            bulk_g2s_hint(stg, p.src_seg[0] + (size_t)src * a1b + (size_t)c * cb, cb, bar, pol);
             if (c == 0)
                 for (int sg = 1; sg < p.n_seg; ++sg)
-                    bulk_g2s(stg + cb + (p.seg_off[sg] - a1b),
-                             p.src_seg[sg] + (size_t)src * p.seg_bytes[sg], p.seg_bytes[sg], bar);
+                    bulk_g2s_hint(stg + cb + (p.seg_off[sg] - a1b),
+                                  p.src_seg[sg] + (size_t)src * p.seg_bytes[sg], p.seg_bytes[sg], bar, pol);
         } else {
             const uint8_t *row = src_whole + (size_t)src * p.row_bytes;
-            bulk_g2s(stg, row + (size_t)c * cb, cb, bar);
-            if (c == 0 && tail) bulk_g2s(stg + cb, row + a1b, tail, bar);
+            bulk_g2s_hint(stg, row + (size_t)c * cb, cb, bar, pol);
+            if (c == 0 && tail) bulk_g2s_hint(stg + cb, row + a1b, tail, bar, pol);
         }
     };
 
